@@ -1,0 +1,255 @@
+"""CPU oracle for the speculative-decode verify matmul -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+library never does, and this package imports nothing from the product.
+
+Everything here is a thin ctypes/numpy wrapper over ``qmm_oracle.c``: the plain
+definition of the verify product (dequantize to fp64, naive triple loop) plus
+the Q4_0 / FP8 quantizers that write the synthetic weight files and the fp32
+Walsh-Hadamard model.  See ``qmm_oracle.c`` for the formulas and the pages each
+one follows.
+
+Pin status (what fixes each function other than itself; see tests/test_oracle_pins.py):
+  decoders (bf16, fp16, e4m3)  -- exhaustive against library casts and closed forms
+  encoders (fp16, e4m3)        -- exhaustive round trips, midpoint ties, library casts
+  Q4_0 quantize / dequant      -- closed form, hand blocks, top-bit-flip identity, bounds
+  FP8 quantize / dequant       -- closed form, library cast, tile bounds
+  FWHT (fp32 and fp64)         -- H H^T = 32 I, unit vectors, involution, fp64 bound
+  verify product               -- M independent GEMVs, brute force vs numpy and exact
+                                  rationals, one-hot and all-ones special cases
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = [
+    "lib", "bf16_to_f64", "f16_to_f64", "e4m3_to_f64", "f32_to_f16_rne", "f32_to_e4m3_sat",
+    "fwht32_f32", "fwht32_f64", "hadamard32_act_f32", "q4_0_quantize", "q4_0_quantize_h32",
+    "q4_0_dequant", "fp8_quantize", "fp8_dequant", "matmul_f64", "verify_rows",
+    "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8",
+]
+
+FMT_Q4_0 = 0
+FMT_FP8 = 1
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+
+def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded oracle library."""
+    L.oracle_bf16_to_f64.restype = ctypes.c_double
+    L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    L.oracle_f16_to_f64.restype = ctypes.c_double
+    L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    L.oracle_e4m3_to_f64.restype = ctypes.c_double
+    L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    L.oracle_f32_to_f16_rne.restype = ctypes.c_uint16
+    L.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
+    L.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    L.oracle_fwht32_f32.argtypes = [_P, _P]
+    L.oracle_fwht32_f64.argtypes = [_P, _P]
+    L.oracle_hadamard32_act_f32.argtypes = [_P, _I64, _INT, _I64, _P]
+    L.oracle_q4_0_quantize.argtypes = [_P, _I64, _I64, _P]
+    L.oracle_q4_0_quantize_h32.argtypes = [_P, _I64, _I64, _P]
+    L.oracle_q4_0_dequant.argtypes = [_P, _I64, _I64, _P]
+    L.oracle_fp8_quantize.argtypes = [_P, _I64, _I64, _P, _P]
+    L.oracle_fp8_dequant.argtypes = [_P, _P, _I64, _I64, _P]
+    L.oracle_matmul_f64.argtypes = [_P, _P, _INT, _I64, _I64, _P, _P]
+    L.oracle_verify_rows.restype = _INT
+    L.oracle_verify_rows.argtypes = [_INT, _P, _P, _I64, _I64, _P, _I64, _INT, _INT, _P,
+                                     _I64, _P, _P]
+    L.oracle_num_threads.restype = _INT
+    L.oracle_set_num_threads.argtypes = [_INT]
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    """Build (if needed) and load the oracle shared library."""
+    global _lib
+    if _lib is None:
+        _lib = _configure(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+# ---------------------------------------------------------------- scalars
+def bf16_to_f64(bits) -> np.ndarray:
+    b = _c(bits, np.uint16).ravel()
+    f = lib().oracle_bf16_to_f64
+    return np.array([f(int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    b = _c(bits, np.uint16).ravel()
+    f = lib().oracle_f16_to_f64
+    return np.array([f(int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    b = _c(codes, np.uint8).ravel()
+    f = lib().oracle_e4m3_to_f64
+    return np.array([f(int(x)) for x in b], dtype=np.float64).reshape(np.shape(codes))
+
+
+def f32_to_f16_rne(x) -> np.ndarray:
+    v = _c(x, np.float32).ravel()
+    f = lib().oracle_f32_to_f16_rne
+    return np.array([f(float(t)) for t in v], dtype=np.uint16).reshape(np.shape(x))
+
+
+def f32_to_e4m3_sat(x) -> np.ndarray:
+    v = _c(x, np.float32).ravel()
+    f = lib().oracle_f32_to_e4m3_sat
+    return np.array([f(float(t)) for t in v], dtype=np.uint8).reshape(np.shape(x))
+
+
+# ---------------------------------------------------------------- Hadamard
+def fwht32_f32(x) -> np.ndarray:
+    v = _c(x, np.float32)
+    assert v.shape[-1] == 32
+    flat = v.reshape(-1, 32)
+    out = np.empty_like(flat)
+    for i in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[i])
+        o = np.empty(32, np.float32)
+        lib().oracle_fwht32_f32(_ptr(row), _ptr(o))
+        out[i] = o
+    return out.reshape(v.shape)
+
+
+def fwht32_f64(x) -> np.ndarray:
+    v = _c(x, np.float64)
+    assert v.shape[-1] == 32
+    flat = v.reshape(-1, 32)
+    out = np.empty_like(flat)
+    for i in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[i])
+        o = np.empty(32, np.float64)
+        lib().oracle_fwht32_f64(_ptr(row), _ptr(o))
+        out[i] = o
+    return out.reshape(v.shape)
+
+
+def hadamard32_act_f32(act_bf16: np.ndarray) -> np.ndarray:
+    """fp32 device model of the activation rotation: [M][K] bf16 bits -> [M][K] fp32."""
+    a = _c(act_bf16, np.uint16)
+    M, K = a.shape
+    assert K % 32 == 0
+    out = np.empty((M, K), np.float32)
+    lib().oracle_hadamard32_act_f32(_ptr(a), K, M, K, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- Q4_0
+def q4_0_quantize(w: np.ndarray) -> np.ndarray:
+    """[N][K] fp32 -> canonical Q4_0 bytes, shape [N][K/32][18] uint8."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    out = np.empty((N, K // 32, 18), np.uint8)
+    lib().oracle_q4_0_quantize(_ptr(w), N, K, _ptr(out))
+    return out
+
+
+def q4_0_quantize_h32(w: np.ndarray) -> np.ndarray:
+    """Rotate each 32-block by H (fp32), divide by 32, quantize to Q4_0."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    out = np.empty((N, K // 32, 18), np.uint8)
+    lib().oracle_q4_0_quantize_h32(_ptr(w), N, K, _ptr(out))
+    return out
+
+
+def q4_0_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    b = _c(blocks, np.uint8)
+    assert b.size == N * (K // 32) * 18
+    out = np.empty((N, K), np.float64)
+    lib().oracle_q4_0_dequant(_ptr(b), N, K, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- FP8
+def fp8_quantize(w: np.ndarray):
+    """[N][K] fp32 -> (codes [N][K] uint8, scales [ceil(N/128)][ceil(K/128)] fp32)."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty(((N + 127) // 128, (K + 127) // 128), np.float32)
+    lib().oracle_fp8_quantize(_ptr(w), N, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def fp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    s = _c(scales, np.float32)
+    N, K = c.shape
+    out = np.empty((N, K), np.float64)
+    lib().oracle_fp8_dequant(_ptr(c), _ptr(s), N, K, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- product
+def matmul_f64(act: np.ndarray, w: np.ndarray, want_s: bool = True):
+    """Naive triple loop: act [M][K] fp64, w [N][K] fp64 -> out [M][N] (and S)."""
+    a = _c(act, np.float64)
+    ww = _c(w, np.float64)
+    M, K = a.shape
+    N = ww.shape[0]
+    assert ww.shape[1] == K
+    out = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64) if want_s else None
+    lib().oracle_matmul_f64(_ptr(a), _ptr(ww), M, N, K, _ptr(out), _ptr(S) if want_s else None)
+    return (out, S) if want_s else out
+
+
+def verify_rows(fmt: int, wbytes: np.ndarray, scales, N: int, K: int, act_bf16: np.ndarray,
+                hadamard: bool = False, rows=None):
+    """Verify product for selected weight rows (all rows when ``rows`` is None).
+
+    Returns (out [M][len(rows)], S [M][len(rows)]) in fp64.
+    """
+    wb = _c(wbytes, np.uint8)
+    sc = _c(scales, np.float32) if scales is not None else None
+    a = _c(act_bf16, np.uint16)
+    M, lda = a.shape
+    if rows is None:
+        r = None
+        nr = N
+    else:
+        r = _c(rows, np.int64)
+        nr = r.size
+    out = np.empty((M, nr), np.float64)
+    S = np.empty((M, nr), np.float64)
+    rc = lib().oracle_verify_rows(fmt, _ptr(wb), _ptr(sc) if sc is not None else None, N, K,
+                                  _ptr(a), lda, M, int(bool(hadamard)),
+                                  _ptr(r) if r is not None else None, nr, _ptr(out), _ptr(S))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_rows failed with {rc}")
+    return out, S
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    lib().oracle_set_num_threads(int(n))

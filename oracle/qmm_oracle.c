@@ -1,0 +1,436 @@
+/*
+ * qmm_oracle.c -- plain CPU oracle for the speculative-decode verify matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * execute this file: only tests/, __graft_entry__.smoke() and the cpu_baseline
+ * leg of bench.py use it.  It shares no code, header, table or helper with the
+ * CUDA library; the two meet only through byte buffers produced by the seeded
+ * input generators.
+ *
+ * What it computes (the plain definition, no blocking, fusion or reordering):
+ *
+ *   out[m][n] = sum_k a[m][k] * w[n][k]          (fp64, k ascending)
+ *   S[m][n]   = sum_k |a[m][k] * w[n][k]|        (tolerance scale)
+ *
+ * where a is the drafted block of M activation rows (bf16, decoded exactly to
+ * fp64) and w is the dequantized weight matrix (fp64).  One target forward
+ * checks the whole drafted block and reads every weight once
+ * ["Qwen3.8-27B on the AMD R9700: up to 227 tok/s", section "A block-diffusion
+ * drafter, verified exactly"]; verification is exact, i.e. the batched result
+ * is the model's own product ["... 227 tok/s", section "What 'lossless' means
+ * here, precisely"].
+ *
+ * Weight formats:
+ *   Q4_0  -- 32-element blocks, one fp16 scale d each, 4-bit codes q stored
+ *            with an offset of 8: w = d * (q - 8)
+ *            ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve, and 4-bit
+ *            activations with a Hadamard rotation", section "Prompt
+ *            processing: 4-bit activations, rotated first"].
+ *            Block bytes: fp16 d (little endian), then 16 bytes qs where byte
+ *            j holds element j in its low nibble and element j+16 in its high
+ *            nibble (the GGUF convention the pages' Q4_0 files use).
+ *   FP8   -- E4M3 codes with one fp32 scale per 128x128 tile:
+ *            w = e4m3(c) * s[n/128][k/128]
+ *            ["r9k: a from-scratch inference engine for Qwen3.8-27B on two
+ *            Radeon AI PRO R9700", opening section].  E4M3 is the OCP "FN"
+ *            variant: bias 7, no infinities, S.1111.111 is NaN, max 448.
+ *
+ * Hadamard variant: each 32-block of an activation row is rotated by the
+ * unnormalised 32-point Walsh-Hadamard matrix H (H[i][j] = (-1)^popcount(i&j)),
+ * and the weights were rotated the same way offline and divided by 32, so the
+ * product is unchanged because H * H^T = 32 I ["Qwen3.8-27B at 45.7 tok/s",
+ * section "Prompt processing: 4-bit activations, rotated first"].  The page
+ * describes the device rotation as "two in-register butterfly steps and three
+ * lane shuffles"; the fp32 model here fixes that order as strides 1,2,4,8,16,
+ * each stage mapping (x, y) -> (x + y, x - y).
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off (no fast-math), see build.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Scalar decoders (closed forms).                                           */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 -> fp64: a bf16 value is the top half of an IEEE binary32 word. */
+double oracle_bf16_to_f64(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* IEEE binary16 -> fp64 by its closed form. */
+double oracle_f16_to_f64(uint16_t h) {
+  int s = (h >> 15) & 1;
+  int e = (h >> 10) & 31;
+  int m = h & 1023;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+  } else if (e == 31) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else {
+    v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  }
+  return s ? -v : v;
+}
+
+/* OCP E4M3 (FN) -> fp64 by its closed form. */
+double oracle_e4m3_to_f64(uint8_t c) {
+  int s = (c >> 7) & 1;
+  int e = (c >> 3) & 15;
+  int m = c & 7;
+  double v;
+  if (e == 15 && m == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)m, -9); /* subnormal: m * 2^-9 */
+  } else {
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  return s ? -v : v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Encoders used by the oracle's own quantizers.                             */
+/* ------------------------------------------------------------------------ */
+
+/* Round a non-negative double that is an exact multiple of 2^-60 or so to the
+ * nearest integer, ties to even.  nearbyint uses the current rounding mode,
+ * which is round-to-nearest-even by default. */
+static double rne_int(double x) { return nearbyint(x); }
+
+/* fp32 -> binary16, round to nearest even, overflow to infinity. */
+uint16_t oracle_f32_to_f16_rne(float xf) {
+  double x = (double)xf;
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double a = fabs(x);
+  if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+  if (isinf(x)) return (uint16_t)(sign | 0x7C00u);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+  int e = e2 - 1;         /* a in [2^e, 2^(e+1)) */
+  if (e < -14) {
+    /* subnormal range: quantum 2^-24 */
+    double q = rne_int(ldexp(a, 24));
+    /* q == 1024 carries into the smallest normal, which has the same bits */
+    return (uint16_t)(sign | (uint16_t)q);
+  }
+  double q = rne_int(ldexp(a, 10 - e)); /* in [1024, 2048] */
+  if (q == 2048.0) {
+    q = 1024.0;
+    e += 1;
+  }
+  if (e > 15) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* fp32 -> E4M3 (FN), round to nearest even, saturating to +-448 ("satfinite":
+ * finite values beyond the largest normal clamp to it; the sign of a value
+ * that rounds to zero is kept). */
+uint8_t oracle_f32_to_e4m3_sat(float xf) {
+  double x = (double)xf;
+  uint8_t sign = signbit(x) ? 0x80u : 0u;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7Fu;
+  if (a >= 448.0) return (uint8_t)(sign | 0x7Eu);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int e = e2 - 1;
+  if (e < -6) {
+    double q = rne_int(ldexp(a, 9)); /* quantum 2^-9, q in [0, 8] */
+    return (uint8_t)(sign | (uint8_t)q); /* q == 8 is the smallest normal */
+  }
+  double q = rne_int(ldexp(a, 3 - e)); /* in [8, 16] */
+  if (q == 16.0) {
+    q = 8.0;
+    e += 1;
+  }
+  /* a < 448 keeps e + 7 <= 15 with mantissa <= 6 (448 = 1.75 * 2^8). */
+  return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)(q - 8.0));
+}
+
+/* ------------------------------------------------------------------------ */
+/* 32-point Walsh-Hadamard transform.                                         */
+/* ------------------------------------------------------------------------ */
+
+/* fp32 device model: strides 1,2,4,8,16; every stage maps (x, y) to
+ * (x + y, x - y) for the index pairs (i, i + h) with (i & h) == 0. */
+void oracle_fwht32_f32(const float* in, float* out) {
+  float v[32];
+  for (int i = 0; i < 32; ++i) v[i] = in[i];
+  for (int h = 1; h < 32; h <<= 1) {
+    for (int i = 0; i < 32; ++i) {
+      if (i & h) continue;
+      float x = v[i], y = v[i + h];
+      v[i] = x + y;
+      v[i + h] = x - y;
+    }
+  }
+  for (int i = 0; i < 32; ++i) out[i] = v[i];
+}
+
+/* Same butterflies in fp64 (exact for inputs with <= 48 significant bits). */
+void oracle_fwht32_f64(const double* in, double* out) {
+  double v[32];
+  for (int i = 0; i < 32; ++i) v[i] = in[i];
+  for (int h = 1; h < 32; h <<= 1) {
+    for (int i = 0; i < 32; ++i) {
+      if (i & h) continue;
+      double x = v[i], y = v[i + h];
+      v[i] = x + y;
+      v[i + h] = x - y;
+    }
+  }
+  for (int i = 0; i < 32; ++i) out[i] = v[i];
+}
+
+/* Rotate every 32-block of M bf16 activation rows with the fp32 model.
+ * act: [M][lda] bf16 bits; out: [M][K] fp32.  K must be a multiple of 32. */
+void oracle_hadamard32_act_f32(const uint16_t* act, int64_t lda, int M, int64_t K,
+                               float* out) {
+  for (int m = 0; m < M; ++m) {
+    for (int64_t b = 0; b < K / 32; ++b) {
+      float blk[32];
+      for (int j = 0; j < 32; ++j)
+        blk[j] = (float)oracle_bf16_to_f64(act[(int64_t)m * lda + 32 * b + j]);
+      oracle_fwht32_f32(blk, out + (int64_t)m * K + 32 * b);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q4_0.                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Quantize one block of 32 fp32 values into 18 bytes.
+ * d32 = (element of largest magnitude, first on ties, with its sign) / -8,
+ * inv = 1/d32 (0 for an all-zero block), q = clamp(round(x * inv) + 8, 0, 15)
+ * with round-half-away-from-zero, stored d = fp16_rne(d32). */
+static void q4_0_quantize_block(const float* x, uint8_t* blk) {
+  float amax = 0.0f, amax_s = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    float ax = fabsf(x[j]);
+    if (ax > amax) {
+      amax = ax;
+      amax_s = x[j];
+    }
+  }
+  float d32 = amax_s / -8.0f;
+  float inv = (d32 != 0.0f) ? 1.0f / d32 : 0.0f;
+  uint8_t q[32];
+  for (int j = 0; j < 32; ++j) {
+    float t = x[j] * inv;
+    int qi = (int)roundf(t) + 8;
+    if (qi < 0) qi = 0;
+    if (qi > 15) qi = 15;
+    q[j] = (uint8_t)qi;
+  }
+  uint16_t d16 = oracle_f32_to_f16_rne(d32);
+  blk[0] = (uint8_t)(d16 & 0xFF);
+  blk[1] = (uint8_t)(d16 >> 8);
+  for (int j = 0; j < 16; ++j) blk[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+/* w: [N][K] fp32 row-major; blocks: N * (K/32) * 18 bytes, row-major over n. */
+void oracle_q4_0_quantize(const float* w, int64_t N, int64_t K, uint8_t* blocks) {
+  int64_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b)
+      q4_0_quantize_block(w + n * K + 32 * b, blocks + (n * nb + b) * 18);
+}
+
+/* The offline weight rotation for the Hadamard variant: every 32-block of a
+ * weight row is rotated with the fp32 butterflies, divided by 32 (a power of
+ * two, exact), then quantized as above. */
+void oracle_q4_0_quantize_h32(const float* w, int64_t N, int64_t K, uint8_t* blocks) {
+  int64_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      float r[32];
+      oracle_fwht32_f32(w + n * K + 32 * b, r);
+      for (int j = 0; j < 32; ++j) r[j] = r[j] * 0.03125f;
+      q4_0_quantize_block(r, blocks + (n * nb + b) * 18);
+    }
+  }
+}
+
+/* Dequantize one weight row to fp64: w = d * (q - 8). */
+static void q4_0_dequant_row(const uint8_t* blocks, int64_t n, int64_t K, double* row) {
+  int64_t nb = K / 32;
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t* blk = blocks + (n * nb + b) * 18;
+    double d = oracle_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+    for (int j = 0; j < 16; ++j) {
+      int lo = blk[2 + j] & 0x0F;
+      int hi = blk[2 + j] >> 4;
+      row[32 * b + j] = d * (double)(lo - 8);
+      row[32 * b + j + 16] = d * (double)(hi - 8);
+    }
+  }
+}
+
+/* Full dequantization, [N][K] fp64. */
+void oracle_q4_0_dequant(const uint8_t* blocks, int64_t N, int64_t K, double* w) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) q4_0_dequant_row(blocks, n, K, w + n * K);
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 with 128x128 fp32 scales.                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Tile (tn, tk) covers rows [128 tn, 128 tn + 128) and columns
+ * [128 tk, 128 tk + 128) of W[N][K] (clipped at the edges).
+ * s = maxabs(tile) / 448 in fp32; code = e4m3_rne_sat(w / s); s == 0 gives
+ * all-zero codes.  scales: [ceil(N/128)][ceil(K/128)]. */
+void oracle_fp8_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes,
+                         float* scales) {
+  int64_t tn_n = (N + 127) / 128, tk_n = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t tn = 0; tn < tn_n; ++tn) {
+    for (int64_t tk = 0; tk < tk_n; ++tk) {
+      int64_t n0 = tn * 128, n1 = n0 + 128 < N ? n0 + 128 : N;
+      int64_t k0 = tk * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+      float amax = 0.0f;
+      for (int64_t n = n0; n < n1; ++n)
+        for (int64_t k = k0; k < k1; ++k) {
+          float a = fabsf(w[n * K + k]);
+          if (a > amax) amax = a;
+        }
+      float s = amax / 448.0f;
+      scales[tn * tk_n + tk] = s;
+      for (int64_t n = n0; n < n1; ++n)
+        for (int64_t k = k0; k < k1; ++k)
+          codes[n * K + k] = (s != 0.0f) ? oracle_f32_to_e4m3_sat(w[n * K + k] / s) : 0u;
+    }
+  }
+}
+
+static void fp8_dequant_row(const uint8_t* codes, const float* scales, int64_t n,
+                            int64_t K, double* row) {
+  int64_t tk_n = (K + 127) / 128;
+  for (int64_t k = 0; k < K; ++k) {
+    double s = (double)scales[(n / 128) * tk_n + k / 128];
+    row[k] = oracle_e4m3_to_f64(codes[n * K + k]) * s;
+  }
+}
+
+void oracle_fp8_dequant(const uint8_t* codes, const float* scales, int64_t N, int64_t K,
+                        double* w) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) fp8_dequant_row(codes, scales, n, K, w + n * K);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The verify matmul: naive triple loop in fp64.                             */
+/* ------------------------------------------------------------------------ */
+
+/* act: [M][K] fp64, w: [N][K] fp64, out/S: [M][N] fp64 (S may be NULL). */
+void oracle_matmul_f64(const double* act, const double* w, int M, int64_t N, int64_t K,
+                       double* out, double* S) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int m = 0; m < M; ++m) {
+      double acc = 0.0, sabs = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double p = act[(int64_t)m * K + k] * w[n * K + k];
+        acc += p;
+        sabs += fabs(p);
+      }
+      out[(int64_t)m * N + n] = acc;
+      if (S) S[(int64_t)m * N + n] = sabs;
+    }
+  }
+}
+
+/* Decode the bf16 activation rows to fp64; in the Hadamard variant rotate each
+ * 32-block exactly in fp64 (sums of 32 bf16 values are exact in fp64). */
+static void decode_act(const uint16_t* act, int64_t lda, int M, int64_t K, int hadamard,
+                       double* a) {
+  for (int m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k)
+      a[(int64_t)m * K + k] = oracle_bf16_to_f64(act[(int64_t)m * lda + k]);
+  if (hadamard) {
+    for (int m = 0; m < M; ++m)
+      for (int64_t b = 0; b < K / 32; ++b) {
+        double* blk = a + (int64_t)m * K + 32 * b;
+        oracle_fwht32_f64(blk, blk);
+      }
+  }
+}
+
+/* Verify product for a selection of weight rows, dequantizing row by row so
+ * that full-size matrices need no [N][K] fp64 buffer.
+ *   fmt: 0 = Q4_0 (wbytes = blocks), 1 = FP8 (wbytes = codes, scales)
+ *   rows: nrows output-feature indices (NULL = all N, nrows ignored)
+ *   out, S: [M][nrows] fp64 (S may be NULL) */
+int oracle_verify_rows(int fmt, const uint8_t* wbytes, const float* scales, int64_t N,
+                       int64_t K, const uint16_t* act, int64_t lda, int M, int hadamard,
+                       const int64_t* rows, int64_t nrows, double* out, double* S) {
+  if (K <= 0 || N <= 0 || M <= 0 || (fmt == 0 && K % 32) || (hadamard && K % 32))
+    return -1;
+  if (!rows) nrows = N;
+  double* a = (double*)malloc(sizeof(double) * (size_t)M * (size_t)K);
+  if (!a) return -2;
+  decode_act(act, lda, M, K, hadamard, a);
+  int err = 0;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!w) {
+#pragma omp atomic write
+      err = -2;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (fmt == 0)
+          q4_0_dequant_row(wbytes, n, K, w);
+        else
+          fp8_dequant_row(wbytes, scales, n, K, w);
+        for (int m = 0; m < M; ++m) {
+          double acc = 0.0, sabs = 0.0;
+          for (int64_t k = 0; k < K; ++k) {
+            double p = a[(int64_t)m * K + k] * w[k];
+            acc += p;
+            sabs += fabs(p);
+          }
+          out[(int64_t)m * nrows + i] = acc;
+          if (S) S[(int64_t)m * nrows + i] = sabs;
+        }
+      }
+      free(w);
+    }
+  }
+  free(a);
+  return err;
+}
+
+/* Number of OpenMP threads a parallel region uses (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
