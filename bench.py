@@ -1,0 +1,522 @@
+"""Benchmark: verify-matmul weight GB/s at M = 1 / 8 / 16 drafted rows.
+
+One "step" is one verify pass of the workload at each of M = 1, 8 and 16:
+the default workload is the Q4_0 attention-projection shape (K = N = 5120),
+streamed through R distinct copies of the weights whose total (R x 14.7 MB)
+is well above the 129 MB L2, so every launch reads its weights from HBM.
+Each M is captured as one CUDA graph of R back-to-back verify calls (the
+activation pre-pass and the verify kernel per call, chained with
+programmatic dependent launch) and timed with CUDA events on the launching
+stream.  value = compressed weight bytes streamed per step / step time.
+
+Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h,
+fp8_mlp, model (64 layers x {qkv, out, gate+up, down}).
+
+Multi-GPU (--gpus N under torchrun): the path shards into independent
+problems, so every rank runs its own replica of the workload with no
+collective on the data path; ranks meet only at the timing barrier and the
+max-over-ranks reduction of the elapsed time ("scaling": "weak").
+
+--impl reference times the CPU oracle (the plain fp64 triple loop) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+WORKLOADS = {
+    # name: (synth shape, hadamard, Ms)
+    "q4_attn": ("q4_attn", False, (1, 8, 16)),
+    "q4_gateup": ("q4_gateup", False, (16,)),
+    "q4_down": ("q4_down", False, (16,)),
+    "q4_gateup_h": ("q4_gateup", True, (16,)),
+    "q4_down_h": ("q4_down", True, (16,)),
+    "fp8_mlp": ("fp8_mlp", False, (1, 8, 16)),
+}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Largest value over all ranks (x itself when there is one rank)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peak_gbs():
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decode_verification_qmm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the verify kernel from the committed ncu summary,
+    or None when it was taken on other kernel sources."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- GPU arm
+def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0):
+    spec = synth.SHAPES[shape_name]
+    N, K = spec["N"], spec["K"]
+    mats = []
+    for r in range(copies):
+        w = synth.weights_cuda(N, K, spec["seed"] + 7919 * r + seed_base)
+        if spec["fmt"] == "q4_0":
+            blocks = q.quantize_q4_0(w, hadamard=hadamard)
+            del w
+            mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=hadamard))
+            del blocks
+        else:
+            codes, scales = q.quantize_fp8(w, hadamard=hadamard)
+            del w
+            mats.append(q.Matrix(q.QMM_FMT_FP8_E4M3_B128, codes, N, K, scales=scales,
+                                 hadamard=hadamard))
+            del codes, scales
+    torch.cuda.synchronize()
+    return mats, spec
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm once outside the graph
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_gpu(args, ws, rank, local):
+    import torch
+    import speculative_decode_verification_qmm_gb300 as q
+    from speculative_decode_verification_qmm_gb300 import synth
+
+    torch.cuda.set_device(local)
+    q.load()
+    dev = torch.device("cuda", local)
+
+    # ---- workload setup (untimed)
+    groups = []  # list of (M, [(mat, act, out)])
+    if args.workload == "model":
+        shape_desc = []
+        acts = {}
+        mats = []
+        for layer in range(synth.MODEL_LAYERS):
+            for j, (name, N, K) in enumerate(synth.MODEL_LAYER):
+                w = synth.weights_cuda(N, K, 4 * layer + j)
+                blocks = q.quantize_q4_0(w)
+                del w
+                mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K))
+                del blocks
+        torch.cuda.synchronize()
+        Ms = synth.MODEL_MS
+        for M in Ms:
+            items = []
+            for m in mats:
+                key = (M, m.K)
+                if key not in acts:
+                    acts[key] = synth.activations_cuda(M, m.K, 10_000 + m.K, outliers=False)
+                out = torch.empty((M, m.N), dtype=torch.float32, device=dev)
+                items.append((m, acts[key], out))
+            groups.append((M, items))
+        per_copy_bytes = sum(m.info()["weight_bytes"] for m in mats)
+        copies = 1
+        workload_desc = (f"whole-model Q4_0 sweep: {synth.MODEL_LAYERS} layers x "
+                         f"{{qkv 10240x5120, out 5120x5120, gate+up 34816x5120, down 5120x17408}}, "
+                         f"{per_copy_bytes / 2**30:.2f} GiB compressed per pass, one pass per M")
+        main_kernel = "verify_kernel<0"
+        dtype = "bf16"
+    else:
+        shape_name, hadamard, Ms = WORKLOADS[args.workload]
+        spec = synth.SHAPES[shape_name]
+        N, K = spec["N"], spec["K"]
+        one = (N * K // 32 * 18) if spec["fmt"] == "q4_0" else (N * K + 4 * (N // 128) * (K // 128))
+        copies = args.copies or max(2, -(-4 * L2_BYTES // one))
+        mats, spec = build_matrices(q, synth, shape_name, hadamard, copies, torch)
+        for M in Ms:
+            act = synth.activations_cuda(M, K, spec["seed"] + 1000, outliers=spec["outliers"])
+            items = [(m, act, torch.empty((M, N), dtype=torch.float32, device=dev)) for m in mats]
+            groups.append((M, items))
+        per_copy_bytes = one
+        fmt_name = "Q4_0" if spec["fmt"] == "q4_0" else "FP8 E4M3 128x128"
+        workload_desc = (f"{fmt_name} verify K={K} N={N}{' Hadamard32' if hadamard else ''}, "
+                         f"M={'/'.join(map(str, Ms))}, {copies} distinct weight copies "
+                         f"({copies * one / 1e6:.0f} MB, > 4x L2) cycled")
+        main_kernel = "verify_kernel<" + ("0" if spec["fmt"] == "q4_0" else "1")
+        dtype = "f16" if (hadamard or spec["fmt"] != "q4_0") else "bf16"
+
+    def run_group(items):
+        for m, act, out in items:
+            q.qmm_verify(m.handle, act, out, act.shape[0])
+
+    graphs = [(M, capture(torch, lambda it=items: run_group(it)), items) for M, items in groups]
+    launches_per_step = sum(2 * len(items) for _, items in groups)
+    bytes_per_step = sum(sum(m.info()["weight_bytes"] for m, _, _ in items) for _, items in groups)
+
+    # ---- warmup
+    for _ in range(args.warmup):
+        for _, g, _ in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    for _, items in groups:
+        for m, _, _ in items:
+            rc = m.sync_status()
+            if rc != q.QMM_OK:
+                raise RuntimeError(f"device status after warmup: {q.qmm_strerror(rc)}")
+
+    # ---- timed region: K steps; per-M events on the launching stream
+    stream = torch.cuda.current_stream()
+    per_m = {M: 0.0 for M, _, _ in graphs}
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        marks = []
+        ev0.record(stream)
+        for _ in range(args.steps):
+            for M, g, _ in graphs:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                marks.append((M, a, b))
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = ev0.elapsed_time(ev1)
+    for M, a, b in marks:
+        per_m[M] += a.elapsed_time(b)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    ms_per_step = total_ms / args.steps
+    total_bytes = sum_over_ranks(bytes_per_step * args.steps, ws, dev)
+    value = total_bytes / (total_ms * 1e-3) / 1e9
+    clk = clocks.summary()
+
+    for _, items in groups:
+        for m, _, _ in items:
+            rc = m.sync_status()
+            if rc != q.QMM_OK:
+                raise RuntimeError(f"device status after timing: {q.qmm_strerror(rc)}")
+
+    peak, peak_kind = measured_peak_gbs()
+    per_launch_bytes = bytes_per_step / (launches_per_step // 2)
+    avg_launch_s = (ms_per_step * 1e-3) / (launches_per_step // 2)
+    achieved = per_launch_bytes / avg_launch_s / 1e9
+    m_breakdown = {}
+    for M, _, items in graphs:
+        b = sum(m.info()["weight_bytes"] for m, _, _ in items)
+        t = per_m[M] / args.steps
+        m_breakdown[str(M)] = {"ms": round(t, 5), "GBps": round(b / (t * 1e-3) / 1e9, 1),
+                               "pct_of_peak": round(100 * b / (t * 1e-3) / 1e9 / peak, 1)}
+
+    # ---- end to end through the host-buffer entry point (pinned buffers)
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for M, items in groups:
+            for m, act, out in items:
+                host.append((m, act.cpu().pin_memory(), torch.empty(out.shape, dtype=torch.float32).pin_memory()))
+        for m, ah, oh in host[: min(len(host), 8)]:
+            m.verify_host(ah, oh)
+        h2d = sum(ah.numel() * 2 for _, ah, _ in host)
+        d2h = sum(oh.numel() * 4 for _, _, oh in host)
+        e2e_steps = max(1, min(args.steps, 3))
+        barrier(ws)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for m, ah, oh in host:
+                m.verify_host(ah, oh)
+        t1 = time.perf_counter()
+        el = max_over_ranks(t1 - t0, ws, dev)
+        e2e_bytes = sum_over_ranks(bytes_per_step * e2e_steps, ws, dev)
+        e2e = {"value": round(e2e_bytes / el / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "api": "qmm_verify_host (pinned host buffers, synchronous per call)"}
+
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": "verify-matmul weight GB/s (% of GB300 HBM peak) at M=1/8/16 draft rows",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic (seeded N(0,0.02) weights quantized on the device, bf16 N(0,1) "
+                "activations with 0.1% x20 outlier channels)",
+        "config": {"workload": workload_desc, "l2": "inputs larger than L2 (distinct weight copies)",
+                   "parallelism": f"replicas x{ws}", "per_M": m_breakdown,
+                   "pct_of_peak": round(100 * value / ws / peak, 1),
+                   "m16_over_m1_time": (round(m_breakdown["16"]["ms"] / m_breakdown["1"]["ms"], 3)
+                                        if "16" in m_breakdown and "1" in m_breakdown else None)},
+        "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (STREAM-style copy)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 3),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch_bytes),
+                     "note": "average launch duration over the timed region (pre-pass included)"},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line, rank
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_sample_rate(budget_s: float, workload: str):
+    """Time the oracle on a bounded row sample of the workload at every M of the
+    step; return (GB/s of weight bytes processed, threads, sample description)."""
+    import numpy as np
+    import oracle as O
+    from speculative_decode_verification_qmm_gb300 import synth
+
+    if workload == "model":
+        shape_name, hadamard, Ms = "q4_attn", False, synth.MODEL_MS
+    else:
+        shape_name, hadamard, Ms = WORKLOADS[workload]
+    spec = synth.SHAPES[shape_name]
+    N, K = spec["N"], spec["K"]
+    rows_n = min(N, 512)
+    w = synth.weights(rows_n, K, spec["seed"])
+    if spec["fmt"] == "q4_0":
+        wb = O.q4_0_quantize_h32(w) if hadamard else O.q4_0_quantize(w)
+        sc, fmt, row_bytes = None, O.FMT_Q4_0, K // 32 * 18
+    else:
+        wb, sc = O.fp8_quantize(w)
+        fmt, row_bytes = O.FMT_FP8, K
+    acts = {M: synth.activations(M, K, spec["seed"] + 1000, outliers=spec["outliers"],
+                                 outlier_seed=spec["seed"] + 2000) for M in Ms}
+    done_bytes, t_total, reps = 0, 0.0, 0
+    while t_total < budget_s or reps == 0:
+        for M in Ms:
+            t0 = time.perf_counter()
+            O.verify_rows(fmt, wb, sc, rows_n, K, acts[M], hadamard=hadamard)
+            t_total += time.perf_counter() - t0
+            done_bytes += rows_n * row_bytes
+        reps += 1
+    sample = (f"{rows_n} of {N} weight rows x K={K}, M={'/'.join(map(str, Ms))}, "
+              f"{reps} pass(es), {t_total:.1f} s")
+    return done_bytes / t_total / 1e9, O.num_threads(), sample
+
+
+def cpu_baseline(args):
+    v, cores, sample = oracle_sample_rate(args.cpu_budget, args.workload)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample_rate(0.0, args.workload)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, sample = oracle_sample_rate(max(1.0, args.cpu_budget / max(1, args.steps)),
+                                              args.workload)
+        vals.append(v)
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(vals)
+    return {
+        "impl": "reference",
+        "metric": "verify-matmul weight GB/s (% of GB300 HBM peak) at M=1/8/16 draft rows",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": f"{args.workload} (CPU oracle on a bounded row sample)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(list(WORKLOADS) + ["model"]), default="q4_attn")
+    ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: >= 4x L2)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line, rank = run_gpu(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

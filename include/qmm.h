@@ -1,0 +1,221 @@
+/*
+ * qmm.h -- C ABI of the GB300 verify matmul for speculative decoding.
+ *
+ * The operation.  One speculative-decoding step checks a whole drafted block
+ * of M token positions with a single batched forward of the target model; in
+ * that forward every weight matrix is read once and applied to all M rows, so
+ * checking 16 positions costs about as much as checking one
+ * ["Qwen3.8-27B on the AMD R9700: up to 227 tok/s", section "A block-diffusion
+ * drafter, verified exactly"].  The hot part of that forward is the skinny
+ * block-quantized matmul this library computes:
+ *
+ *     out[m][n] = sum_k act[m][k] * W[n][k]       1 <= M <= 16, fp32 accumulate
+ *
+ * with W stored compressed:
+ *   QMM_FMT_Q4_0           32-element blocks, one fp16 scale d per block, 4-bit
+ *                          codes q with an offset of 8: W = d * (q - 8)
+ *                          ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve,
+ *                          and 4-bit activations with a Hadamard rotation",
+ *                          section "Prompt processing: 4-bit activations,
+ *                          rotated first"].
+ *   QMM_FMT_FP8_E4M3_B128  E4M3 (OCP FN) codes with one fp32 scale per 128x128
+ *                          tile: W = e4m3(c) * s[n/128][k/128]
+ *                          ["r9k: a from-scratch inference engine for
+ *                          Qwen3.8-27B on two Radeon AI PRO R9700", opening
+ *                          section].
+ * and optionally QMM_FLAG_HADAMARD32: every 32-block of each activation row is
+ * rotated on the device by the unnormalised 32-point Walsh-Hadamard matrix H
+ * (strides 1,2,4,8,16, each stage (x, y) -> (x + y, x - y), fp32), for weights
+ * that were rotated the same way offline and divided by 32 (see
+ * qmm_quantize_q4_0), so the product equals the unrotated one
+ * ["Qwen3.8-27B at 45.7 tok/s ...", same section].
+ *
+ * Conventions for every entry point:
+ *   - Return value: QMM_OK (0) or one of the QMM_ERR_* codes below.  No call
+ *     throws, aborts or prints.  qmm_strerror() names a code.
+ *   - "device" pointers are CUDA global-memory pointers of the current device;
+ *     "host" pointers are ordinary (pageable or pinned) host memory.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls documented as asynchronous only enqueue work on it.
+ *   - The caller owns every buffer it passes; the library never frees caller
+ *     memory and keeps no pointer to it after the call returns.
+ *   - bf16 activations are passed as uint16_t bit patterns.
+ */
+#ifndef QMM_H_
+#define QMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMM_ABI_VERSION 1
+
+/* ---- status codes ------------------------------------------------------- */
+enum {
+  QMM_OK = 0,
+  QMM_ERR_INVALID_ARG = 1, /* NULL pointer, bad enum, bad struct_size, bad flag */
+  QMM_ERR_SHAPE = 2,       /* N or K not accepted by the format (see qmm_desc)   */
+  QMM_ERR_M_RANGE = 3,     /* M outside [1, 16]                                 */
+  QMM_ERR_ALIGN = 4,       /* pointer alignment or leading dimension rejected   */
+  QMM_ERR_CUDA = 5,        /* a CUDA call failed; see qmm_last_cuda_error()     */
+  QMM_ERR_TIMEOUT = 6,     /* a bounded device wait expired (qmm_sync_status)   */
+  QMM_ERR_STATE = 7,       /* NULL, destroyed or otherwise unusable handle      */
+  QMM_ERR_DEVICE = 8       /* no sm_103 device, or the handle's device is not current */
+};
+
+/* ---- formats and flags ---------------------------------------------------- */
+typedef enum { QMM_FMT_Q4_0 = 0, QMM_FMT_FP8_E4M3_B128 = 1 } qmm_format;
+
+enum {
+  /* Rotate each 32-block of the activations on the device (weights must have
+   * been rotated offline the same way and divided by 32). */
+  QMM_FLAG_HADAMARD32 = 1u << 0,
+  /* Use the CUDA-core (FP32 FMA) verify kernel instead of the tensor-core one.
+   * Same results within the tolerance; kept as the measured baseline. */
+  QMM_FLAG_SIMT = 1u << 1
+};
+
+/* Description of one weight matrix W[N][K]. */
+typedef struct {
+  uint32_t struct_size;      /* = sizeof(qmm_desc)                              */
+  uint32_t format;           /* qmm_format                                      */
+  int64_t N;                 /* output features (rows of W), N >= 1             */
+  int64_t K;                 /* input features; Q4_0: K % 32 == 0;
+                                FP8: N % 128 == 0 and K % 128 == 0              */
+  uint32_t flags;            /* QMM_FLAG_*                                      */
+  int32_t weights_on_device; /* 1: weights/scales are device pointers; 0: host  */
+  const void* weights;       /* Q4_0: N*(K/32) blocks of 18 bytes, row-major over
+                                n then block: fp16 d (little endian), then 16 bytes
+                                where byte j holds element j in its low nibble and
+                                element j+16 in its high nibble.
+                                FP8: uint8 E4M3 codes [N][K], row-major.        */
+  const float* scales;       /* FP8: fp32 [N/128][K/128] row-major; Q4_0: NULL  */
+  int32_t k_splits;          /* 0: the planner chooses; > 0: use this many K splits
+                                (tuning and tests; clamped to the stage count)  */
+} qmm_desc;
+
+/* Opaque handle: owns the device copy of W (repacked for the kernels) and the
+ * per-handle scratch.  A handle may be used from one stream at a time. */
+typedef struct qmm_handle* qmm_t;
+
+/* What a handle holds and how it will launch (for benchmarks and tests). */
+typedef struct {
+  uint32_t struct_size;          /* = sizeof(qmm_info), set by the caller      */
+  uint32_t format, flags;
+  int64_t N, K;
+  int64_t weight_bytes;          /* compressed bytes of W as the format defines
+                                    them: Q4_0 N*K*18/32; FP8 N*K + 4*(N/128)*(K/128) */
+  int64_t device_weight_bytes;   /* bytes of the repacked device copy (with padding) */
+  int64_t scratch_bytes;         /* per-handle scratch                          */
+  int32_t n_tiles;               /* row tiles of the verify grid                */
+  int32_t k_splits;              /* K splits of the verify grid                 */
+  int32_t ctas;                  /* CTAs per verify launch                      */
+  int32_t stages_per_cta;        /* pipeline stages each CTA streams            */
+  int32_t stage_bytes;           /* weight bytes of one stage                   */
+  int32_t pipeline_depth;        /* stages in flight per CTA                    */
+  int32_t device;                /* CUDA device ordinal the handle lives on     */
+  int32_t sm_count;
+} qmm_info;
+
+/* ---- lifetime --------------------------------------------------------------- */
+
+/* Create a handle for W.  Validates the description, allocates the device copy
+ * and scratch, and repacks W on the device (from host memory if
+ * weights_on_device == 0).  Returns after the repack finished on `stream`, so
+ * the caller may free its weight buffers right away.
+ * Errors: INVALID_ARG (NULL out/desc/weights, unknown format or flag, FP8
+ * without scales), SHAPE (see qmm_desc), DEVICE, CUDA (allocation or copy
+ * failure; nothing is leaked and *out is set to NULL). */
+int qmm_create(qmm_t* out, const qmm_desc* desc, void* stream);
+
+/* Destroy a handle and free everything it owns (synchronises its device work
+ * first).  NULL is accepted.  Using a handle after this returns QMM_ERR_STATE. */
+int qmm_destroy(qmm_t h);
+
+/* ---- the verify product ------------------------------------------------------ */
+
+/* out[m][n] = sum_k act[m][k] * W[n][k] for 0 <= m < M, 0 <= n < N.
+ *   act : device, bf16 bits, row m at act + m*lda; 16-byte aligned, lda >= K,
+ *         lda % 8 == 0 (so every row starts on a 16-byte boundary).
+ *   out : device, fp32, row m at out + m*ldo; 16-byte aligned, ldo >= N.  Fully
+ *         overwritten (the caller does not clear it); rows >= M are untouched.
+ * Asynchronous on `stream`: enqueues the activation pre-pass and the verify
+ * kernel and returns; never synchronises.  Row m's result is bit-identical for
+ * every M (the same kernel and summation order serves M = 1..16).
+ * Errors: STATE, M_RANGE, INVALID_ARG (NULL act/out), ALIGN, CUDA (launch). */
+int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
+               int M, void* stream);
+
+/* The same product for callers that hold host buffers: copies act to the
+ * handle's device staging buffer, runs qmm_verify, copies the result back into
+ * out_host and waits for `stream` before returning (synchronous).  Pinned
+ * host memory gives the fastest copies.  Same argument rules as qmm_verify
+ * except that the 16-byte alignment rule does not apply to host pointers. */
+int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_host,
+                    int64_t ldo, int M, void* stream);
+
+/* ---- status ------------------------------------------------------------------ */
+
+/* Wait for `stream`, then read and clear the handle's device error word.
+ * Returns QMM_OK, QMM_ERR_TIMEOUT (a kernel gave up on a bounded wait; its
+ * output is undefined and the handle's device state has been reset), or
+ * QMM_ERR_CUDA (the stream reported an error). */
+int qmm_sync_status(qmm_t h, void* stream);
+
+/* The last cudaError_t recorded on the handle (0 if none); NULL handle gives
+ * the last error recorded by a handle-less call. */
+int qmm_last_cuda_error(qmm_t h);
+
+/* Fill *info (info->struct_size must be set). */
+int qmm_get_info(qmm_t h, qmm_info* info);
+
+/* Static, NUL-terminated name of a status code. */
+const char* qmm_strerror(int code);
+
+/* ---- test and tool entry points ------------------------------------------------ */
+
+/* Dequantize the handle's W into w_out (device, fp32 [N][K] row-major), exactly
+ * (Q4_0: fp32(d) * (q - 8); FP8: fp32(e4m3) * s, one fp32 multiply).  Async. */
+int qmm_dequantize(qmm_t h, float* w_out, void* stream);
+
+/* Rotate every 32-block of M bf16 rows with the fp32 butterflies described at
+ * the top of this file.  act: device [M][lda] bf16 (16-byte aligned, lda % 8 ==
+ * 0, lda >= K); act_out: device fp32 [M][K].  K % 32 == 0, 1 <= M.  Async. */
+int qmm_hadamard32(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K,
+                   void* stream);
+
+/* Quantize fp32 weights w (device [N][K]) into Q4_0 blocks (device, N*(K/32)*18
+ * bytes, layout as in qmm_desc).  Per block: d32 = (element of largest
+ * magnitude, first on ties, with its sign) / -8; q = clamp(roundf(w / d32) + 8,
+ * 0, 15) using w * (1/d32); stored d = fp16 round-to-nearest-even of d32.
+ * With QMM_FLAG_HADAMARD32 in flags every 32-block is first rotated with the
+ * fp32 butterflies and divided by 32 (the offline half of the Hadamard
+ * variant).  K % 32 == 0.  Async. */
+int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
+                      void* stream);
+
+/* Quantize fp32 weights w (device [N][K]) to E4M3 codes (device [N][K]) and
+ * fp32 scales (device [N/128][K/128]): per 128x128 tile s = maxabs / 448 and
+ * code = e4m3 round-to-nearest-even of w / s, saturated to +-448 (s == 0 gives
+ * zero codes).  QMM_FLAG_HADAMARD32 rotates each 32-block first (and divides
+ * by 32).  N % 128 == 0, K % 128 == 0.  Async. */
+int qmm_quantize_fp8(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* codes,
+                     float* scales, void* stream);
+
+/* Test hook: limit, in nanoseconds, of every bounded device wait of this
+ * handle's kernels (default 2e9).  0 makes every such wait give up at once,
+ * which exercises the timeout path without hanging anything; the kernels
+ * still drain their own copies in flight before returning. */
+int qmm_debug_set_wait_limit(qmm_t h, int64_t ns);
+
+/* Test hook: make the n-th device allocation made by qmm_create from now on
+ * fail as if cudaMalloc had failed (n = 0 disables; the hook fires once). */
+int qmm_debug_fail_allocs(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H_ */

@@ -1,1 +1,224 @@
-"""GB300-native verify matmul for speculative decoding (placeholder; binding follows)."""
+"""GB300-native verify matmul for speculative decoding.
+
+Python binding of ``include/qmm.h``: the functions below keep the C names and
+only marshal arguments (torch tensors -> device pointers, the current CUDA
+stream); every step of the computation runs in ``libqmm.so``'s kernels.
+
+    out[m][n] = sum_k act[m][k] * W[n][k],  1 <= M <= 16
+
+with W in Q4_0 (32-element blocks, fp16 scale, 4-bit codes offset by 8) or
+FP8 E4M3 with 128x128 fp32 scales, optionally with the 32-point Hadamard
+rotation of the activations for weights rotated offline.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_ARG,
+                   QMM_ERR_M_RANGE, QMM_ERR_SHAPE, QMM_ERR_STATE, QMM_ERR_TIMEOUT,
+                   QMM_FLAG_HADAMARD32, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
+                   QMM_OK, QmmError, load, qmm_desc, qmm_info)
+
+__all__ = [
+    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_host", "qmm_sync_status",
+    "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
+    "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
+    "QmmError", "load",
+    "QMM_OK", "QMM_ERR_INVALID_ARG", "QMM_ERR_SHAPE", "QMM_ERR_M_RANGE", "QMM_ERR_ALIGN",
+    "QMM_ERR_CUDA", "QMM_ERR_TIMEOUT", "QMM_ERR_STATE", "QMM_ERR_DEVICE",
+    "QMM_FMT_Q4_0", "QMM_FMT_FP8_E4M3_B128", "QMM_FLAG_HADAMARD32", "QMM_FLAG_SIMT",
+]
+
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+def _check(func: str, rc: int):
+    if rc != QMM_OK:
+        raise QmmError(func, rc)
+
+
+# ------------------------------------------------------------------ raw C names
+def qmm_strerror(code: int) -> str:
+    return load().qmm_strerror(code).decode()
+
+
+def qmm_last_cuda_error(h=None) -> int:
+    return load().qmm_last_cuda_error(h)
+
+
+def qmm_create(fmt: int, weights, N: int, K: int, scales=None, flags: int = 0,
+               k_splits: int = 0, stream=None) -> int:
+    """Create a handle.  ``weights``/``scales`` are CUDA tensors (device) or CPU
+    tensors / numpy arrays (host); returns the opaque handle as an int."""
+    import numpy as np
+    d = qmm_desc()
+    d.struct_size = ctypes.sizeof(qmm_desc)
+    d.format = fmt
+    d.N = N
+    d.K = K
+    d.flags = flags
+    d.k_splits = k_splits
+    keep = []
+
+    def addr(x):
+        if x is None:
+            return None, 0
+        if isinstance(x, np.ndarray):
+            a = np.ascontiguousarray(x)
+            keep.append(a)
+            return a.ctypes.data, 0
+        t = x.contiguous()
+        keep.append(t)
+        return _ptr(t), int(t.is_cuda)
+
+    d.weights, on_dev = addr(weights)
+    sc, on_dev_s = addr(scales)
+    d.scales = sc
+    if scales is not None and on_dev_s != on_dev:
+        raise ValueError("weights and scales must both be on the device or both on the host")
+    d.weights_on_device = on_dev
+    h = ctypes.c_void_p()
+    _check("qmm_create", load().qmm_create(ctypes.byref(h), ctypes.byref(d), _stream_ptr(stream)))
+    return h.value
+
+
+def qmm_destroy(h) -> None:
+    _check("qmm_destroy", load().qmm_destroy(h))
+
+
+def qmm_verify(h, act, out, M: int, stream=None) -> None:
+    """act: CUDA bf16 [M, lda>=K]; out: CUDA fp32 [M, ldo>=N]; asynchronous."""
+    _check("qmm_verify", load().qmm_verify(h, _ptr(act), act.stride(0), _ptr(out), out.stride(0),
+                                           M, _stream_ptr(stream)))
+
+
+def qmm_verify_host(h, act, out, M: int, stream=None) -> None:
+    """act: CPU bf16 [M, K] (pinned is fastest); out: CPU fp32 [M, N]; synchronous."""
+    _check("qmm_verify_host", load().qmm_verify_host(h, _ptr(act), act.stride(0), _ptr(out),
+                                                     out.stride(0), M, _stream_ptr(stream)))
+
+
+def qmm_sync_status(h, stream=None) -> int:
+    return load().qmm_sync_status(h, _stream_ptr(stream))
+
+
+def qmm_get_info(h) -> dict:
+    info = qmm_info()
+    info.struct_size = ctypes.sizeof(qmm_info)
+    _check("qmm_get_info", load().qmm_get_info(h, ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in qmm_info._fields_ if name != "struct_size"}
+
+
+def qmm_dequantize(h, w_out, stream=None) -> None:
+    _check("qmm_dequantize", load().qmm_dequantize(h, _ptr(w_out), _stream_ptr(stream)))
+
+
+def qmm_hadamard32(act, act_out, M: int, K: int, stream=None) -> None:
+    _check("qmm_hadamard32", load().qmm_hadamard32(_ptr(act), act.stride(0), _ptr(act_out), M, K,
+                                                   _stream_ptr(stream)))
+
+
+def qmm_quantize_q4_0(w, blocks, flags: int = 0, stream=None) -> None:
+    N, K = w.shape
+    _check("qmm_quantize_q4_0", load().qmm_quantize_q4_0(_ptr(w), N, K, flags, _ptr(blocks),
+                                                         _stream_ptr(stream)))
+
+
+def qmm_quantize_fp8(w, codes, scales, flags: int = 0, stream=None) -> None:
+    N, K = w.shape
+    _check("qmm_quantize_fp8", load().qmm_quantize_fp8(_ptr(w), N, K, flags, _ptr(codes),
+                                                       _ptr(scales), _stream_ptr(stream)))
+
+
+def qmm_debug_set_wait_limit(h, ns: int) -> None:
+    _check("qmm_debug_set_wait_limit", load().qmm_debug_set_wait_limit(h, ns))
+
+
+def qmm_debug_fail_allocs(n: int) -> None:
+    _check("qmm_debug_fail_allocs", load().qmm_debug_fail_allocs(n))
+
+
+# ------------------------------------------------------------------ convenience
+def quantize_q4_0(w, hadamard: bool = False, stream=None):
+    """CUDA fp32 [N, K] -> CUDA uint8 [N, K/32, 18] Q4_0 blocks (device quantizer)."""
+    import torch
+    N, K = w.shape
+    blocks = torch.empty((N, K // 32, 18), dtype=torch.uint8, device=w.device)
+    qmm_quantize_q4_0(w.contiguous(), blocks, QMM_FLAG_HADAMARD32 if hadamard else 0, stream)
+    return blocks
+
+
+def quantize_fp8(w, hadamard: bool = False, stream=None):
+    """CUDA fp32 [N, K] -> (uint8 codes [N, K], fp32 scales [N/128, K/128])."""
+    import torch
+    N, K = w.shape
+    codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    qmm_quantize_fp8(w.contiguous(), codes, scales, QMM_FLAG_HADAMARD32 if hadamard else 0, stream)
+    return codes, scales
+
+
+def hadamard32(act, stream=None):
+    """CUDA bf16 [M, K] -> CUDA fp32 [M, K], every 32-block rotated."""
+    import torch
+    M, K = act.shape
+    out = torch.empty((M, K), dtype=torch.float32, device=act.device)
+    qmm_hadamard32(act, out, M, K, stream)
+    return out
+
+
+class Matrix:
+    """One weight matrix on the device, ready for repeated verify calls."""
+
+    def __init__(self, fmt: int, weights, N: int, K: int, scales=None, hadamard: bool = False,
+                 simt: bool = False, k_splits: int = 0, stream=None):
+        flags = (QMM_FLAG_HADAMARD32 if hadamard else 0) | (QMM_FLAG_SIMT if simt else 0)
+        self.N, self.K, self.fmt = N, K, fmt
+        self.handle = qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream)
+
+    def verify(self, act, out=None, stream=None):
+        import torch
+        M = act.shape[0]
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.float32, device=act.device)
+        qmm_verify(self.handle, act, out, M, stream)
+        return out
+
+    def verify_host(self, act, out=None, stream=None):
+        import torch
+        M = act.shape[0]
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.float32)
+        qmm_verify_host(self.handle, act, out, M, stream)
+        return out
+
+    def dequantize(self, stream=None):
+        import torch
+        w = torch.empty((self.N, self.K), dtype=torch.float32, device="cuda")
+        qmm_dequantize(self.handle, w, stream)
+        return w
+
+    def info(self) -> dict:
+        return qmm_get_info(self.handle)
+
+    def sync_status(self, stream=None) -> int:
+        return qmm_sync_status(self.handle, stream)
+
+    def close(self):
+        if self.handle:
+            qmm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

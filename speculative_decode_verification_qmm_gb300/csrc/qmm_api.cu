@@ -1,0 +1,488 @@
+// qmm_api.cu -- the C ABI (include/qmm.h): handles, validation, the launch
+// planner, device repack at create time, and the asynchronous verify call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <unordered_set>
+
+#include "../../include/qmm.h"
+#include "qmm_kernels.h"
+
+using namespace qmm;
+
+namespace {
+
+constexpr uint64_t HANDLE_MAGIC = 0x514D4D5645524946ull;  // "QMMVERIF"
+constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+// Planner constants: HBM copy bandwidth of the part and what one CTA with its
+// pipeline full sustains (both only rank candidate plans; see plan()).
+constexpr double PLAN_HBM_BPS = 6.8e12;
+constexpr double PLAN_CTA_BPS = 45e9;
+constexpr double PLAN_FIXUP_S = 0.6e-6;
+constexpr double PLAN_L2_BPS = 10e12;
+
+struct Plan {
+  int n_tiles = 0, S = 1, spc = 1, stage_k = 0, stage_bytes = 0, depth = 0;
+  int64_t nst = 0;  // stages per row tile before padding
+};
+
+}  // namespace
+
+struct qmm_handle {
+  uint64_t magic = 0;
+  int device = 0;
+  int sm_count = 0;
+  int fmt = 0;
+  uint32_t flags = 0;
+  int64_t N = 0, K = 0;
+  Plan plan;
+  uint8_t* wdev = nullptr;
+  size_t wdev_bytes = 0;
+  uint16_t* act_scratch = nullptr;
+  size_t act_bytes = 0;
+  float* out_scale = nullptr;  // [MAX_M][S]
+  float* partial = nullptr;    // [n_tiles][S][MAX_M][TILE_N]
+  size_t partial_bytes = 0;
+  int* counters = nullptr;     // [n_tiles]
+  int* status = nullptr;       // device error word
+  uint16_t* stage_act = nullptr;  // host-buffer path: [MAX_M][act_pitch]
+  int64_t stage_act_pitch = 0;
+  float* stage_out = nullptr;     // [MAX_M][N]
+  uint64_t wait_limit_ns = DEFAULT_WAIT_LIMIT_NS;
+  int last_cuda_error = 0;
+};
+
+namespace {
+
+std::mutex g_mu;
+std::unordered_set<qmm_handle*>& live_handles() {
+  static std::unordered_set<qmm_handle*> s;
+  return s;
+}
+std::atomic<int> g_fail_allocs{0};
+std::atomic<int> g_last_error{0};
+
+bool is_live(qmm_handle* h) {
+  if (!h) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return live_handles().count(h) != 0 && h->magic == HANDLE_MAGIC;
+}
+
+// g_fail_allocs > 0 counts down the allocations until the one that fails.
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  int n = g_fail_allocs.load();
+  while (n > 0) {
+    if (g_fail_allocs.compare_exchange_weak(n, n - 1)) {
+      if (n == 1) return cudaErrorMemoryAllocation;
+      break;
+    }
+  }
+  if (bytes == 0) bytes = 16;
+  return cudaMalloc(p, bytes);
+}
+
+int cuda_fail(qmm_handle* h, cudaError_t e) {
+  if (h) h->last_cuda_error = (int)e;
+  g_last_error.store((int)e);
+  return QMM_ERR_CUDA;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Choose the K split count.  Candidates keep every CTA resident in one wave
+// (two CTAs per SM); each is scored by the time to stream its padded bytes at
+// min(HBM bandwidth, CTAs x per-CTA rate) plus a fixed cost and the partial
+// traffic when the splits need the last-CTA reduction.
+Plan make_plan(int fmt, int64_t N, int64_t K, int sm_count, int forced_splits) {
+  Plan p;
+  p.stage_k = fmt == 0 ? Q4_STAGE_K : F8_STAGE_K;
+  p.stage_bytes = fmt == 0 ? Q4_STAGE_BYTES : F8_STAGE_BYTES;
+  p.depth = fmt == 0 ? q4_pipeline_depth() : fp8_pipeline_depth();
+  p.n_tiles = (int)ceil_div(N, TILE_N);
+  p.nst = ceil_div(K, p.stage_k);
+  auto fix = [&](int S) {
+    int64_t spc = ceil_div(p.nst, S);
+    p.spc = (int)spc;
+    p.S = (int)ceil_div(p.nst, spc);
+  };
+  if (forced_splits > 0) {
+    fix((int)(forced_splits < p.nst ? forced_splits : p.nst));
+    return p;
+  }
+  const int64_t max_ctas = 2ll * sm_count;
+  double best = 1e30;
+  int best_s = 1;
+  for (int S = 1; S <= 64 && S <= p.nst; ++S) {
+    const int64_t spc = ceil_div(p.nst, S);
+    if (ceil_div(p.nst, spc) != S) continue;
+    const int64_t ctas = (int64_t)p.n_tiles * S;
+    if (S > 1 && ctas > max_ctas) break;
+    const double bytes = (double)ctas * spc * p.stage_bytes;
+    double rate = (double)ctas * PLAN_CTA_BPS;
+    if (rate > PLAN_HBM_BPS) rate = PLAN_HBM_BPS;
+    double t = bytes / rate;
+    if (S > 1) t += PLAN_FIXUP_S + (double)ctas * TILE_N * MAX_M * 4 * 2 / PLAN_L2_BPS;
+    if (t < best * 0.999) {
+      best = t;
+      best_s = S;
+    }
+  }
+  fix(best_s);
+  return p;
+}
+
+void free_handle(qmm_handle* h) {
+  if (!h) return;
+  int old = -1;
+  cudaGetDevice(&old);
+  if (old != h->device) cudaSetDevice(h->device);
+  cudaFree(h->wdev);
+  cudaFree(h->act_scratch);
+  cudaFree(h->out_scale);
+  cudaFree(h->partial);
+  cudaFree(h->counters);
+  cudaFree(h->status);
+  cudaFree(h->stage_act);
+  cudaFree(h->stage_out);
+  if (old >= 0 && old != h->device) cudaSetDevice(old);
+  h->magic = 0;
+  delete h;
+}
+
+int check_device(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) return QMM_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+    return QMM_ERR_DEVICE;
+  if (major != 10 || minor != 3) return QMM_ERR_DEVICE;
+  return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qmm_strerror(int code) {
+  switch (code) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_INVALID_ARG: return "QMM_ERR_INVALID_ARG";
+    case QMM_ERR_SHAPE: return "QMM_ERR_SHAPE";
+    case QMM_ERR_M_RANGE: return "QMM_ERR_M_RANGE";
+    case QMM_ERR_ALIGN: return "QMM_ERR_ALIGN";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
+    case QMM_ERR_STATE: return "QMM_ERR_STATE";
+    case QMM_ERR_DEVICE: return "QMM_ERR_DEVICE";
+    default: return "QMM_ERR_UNKNOWN";
+  }
+}
+
+int qmm_debug_fail_allocs(int n) {
+  if (n < 0) return QMM_ERR_INVALID_ARG;
+  g_fail_allocs.store(n);
+  return QMM_OK;
+}
+
+int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
+  if (!out) return QMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
+  if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
+  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
+  if (d->k_splits < 0) return QMM_ERR_INVALID_ARG;
+  const int fmt = (int)d->format;
+  if (fmt == 1 && !d->scales) return QMM_ERR_INVALID_ARG;
+  if (fmt == 1 && (d->flags & QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
+  if (d->N < 1 || d->K < 1) return QMM_ERR_SHAPE;
+  if (fmt == 0 && d->K % 32) return QMM_ERR_SHAPE;
+  if (fmt == 1 && (d->N % 128 || d->K % 128)) return QMM_ERR_SHAPE;
+  if (d->N > (1ll << 31) || d->K > (1ll << 31)) return QMM_ERR_SHAPE;
+  int dev = 0, sms = 0;
+  int rc = check_device(&dev, &sms);
+  if (rc != QMM_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  qmm_handle* h = new qmm_handle();
+  h->device = dev;
+  h->sm_count = sms;
+  h->fmt = fmt;
+  h->flags = d->flags;
+  h->N = d->N;
+  h->K = d->K;
+  h->plan = make_plan(fmt, d->N, d->K, sms, d->k_splits);
+  const Plan& p = h->plan;
+  const int64_t stages_total = (int64_t)p.S * p.spc;
+
+  cudaError_t e = fmt == 0 ? prepare_q4_attributes() : prepare_fp8_attributes();
+  if (e != cudaSuccess) {
+    free_handle(h);
+    return cuda_fail(nullptr, e);
+  }
+  h->wdev_bytes = (size_t)p.n_tiles * stages_total * p.stage_bytes;
+  h->act_bytes = (size_t)stages_total * act_stage_bytes(p.stage_k);
+  h->partial_bytes = (size_t)p.n_tiles * p.S * MAX_M * TILE_N * sizeof(float);
+  h->stage_act_pitch = ceil_div(d->K, 8) * 8;
+  void* tmp_w = nullptr;
+  void* tmp_s = nullptr;
+#define QMM_ALLOC(ptr, bytes)                                   \
+  do {                                                          \
+    void* _p = nullptr;                                         \
+    cudaError_t _e = dev_alloc(&_p, (bytes));                   \
+    if (_e != cudaSuccess) {                                    \
+      cudaGetLastError();                                       \
+      cudaFree(tmp_w);                                          \
+      cudaFree(tmp_s);                                          \
+      free_handle(h);                                           \
+      return cuda_fail(nullptr, _e);                            \
+    }                                                           \
+    ptr = reinterpret_cast<decltype(ptr)>(_p);                  \
+  } while (0)
+  QMM_ALLOC(h->wdev, h->wdev_bytes);
+  QMM_ALLOC(h->act_scratch, h->act_bytes);
+  QMM_ALLOC(h->out_scale, (size_t)MAX_M * p.S * sizeof(float));
+  QMM_ALLOC(h->partial, h->partial_bytes);
+  QMM_ALLOC(h->counters, (size_t)p.n_tiles * sizeof(int));
+  QMM_ALLOC(h->status, sizeof(int));
+  QMM_ALLOC(h->stage_act, (size_t)MAX_M * h->stage_act_pitch * sizeof(uint16_t));
+  QMM_ALLOC(h->stage_out, (size_t)MAX_M * d->N * sizeof(float));
+
+  const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(d->weights);
+  const float* ssrc = d->scales;
+  const size_t wbytes = fmt == 0 ? (size_t)d->N * (d->K / 32) * 18 : (size_t)d->N * d->K;
+  const size_t sbytes = fmt == 1 ? (size_t)(d->N / 128) * (d->K / 128) * sizeof(float) : 0;
+  if (!d->weights_on_device) {
+    QMM_ALLOC(tmp_w, wbytes);
+    if ((e = cudaMemcpyAsync(tmp_w, d->weights, wbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+      goto fail;
+    wsrc = reinterpret_cast<const uint8_t*>(tmp_w);
+    if (fmt == 1) {
+      QMM_ALLOC(tmp_s, sbytes);
+      if ((e = cudaMemcpyAsync(tmp_s, d->scales, sbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        goto fail;
+      ssrc = reinterpret_cast<const float*>(tmp_s);
+    }
+  }
+#undef QMM_ALLOC
+  if ((e = launch_repack(fmt, wsrc, ssrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st)) != cudaSuccess)
+    goto fail;
+  if ((e = cudaMemsetAsync(h->act_scratch, 0, h->act_bytes, st)) != cudaSuccess) goto fail;
+  if ((e = cudaMemsetAsync(h->counters, 0, (size_t)p.n_tiles * sizeof(int), st)) != cudaSuccess) goto fail;
+  if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) goto fail;
+  cudaFree(tmp_w);
+  cudaFree(tmp_s);
+  h->magic = HANDLE_MAGIC;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    live_handles().insert(h);
+  }
+  *out = h;
+  return QMM_OK;
+fail:
+  cudaFree(tmp_w);
+  cudaFree(tmp_s);
+  free_handle(h);
+  return cuda_fail(nullptr, e);
+}
+
+int qmm_destroy(qmm_t h) {
+  if (!h) return QMM_OK;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!live_handles().count(h)) return QMM_ERR_STATE;
+    live_handles().erase(h);
+  }
+  free_handle(h);
+  return QMM_OK;
+}
+
+int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+               void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
+  if (!act || !out) return QMM_ERR_INVALID_ARG;
+  if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || lda < h->K || (lda & 7) || ldo < h->N)
+    return QMM_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Plan& p = h->plan;
+  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
+  const bool f16 = had || h->fmt == 1;
+
+  PrepParams pp;
+  pp.act = act;
+  pp.lda = lda;
+  pp.out = h->act_scratch;
+  pp.out_scale = h->out_scale;
+  pp.K = h->K;
+  pp.M = M;
+  pp.S = p.S;
+  pp.spc = p.spc;
+  pp.stage_k = p.stage_k;
+  cudaError_t e = launch_act_prep(pp, f16, had, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+
+  VerifyParams vp;
+  vp.wdev = h->wdev;
+  vp.act = reinterpret_cast<const uint8_t*>(h->act_scratch);
+  vp.out_scale = h->out_scale;
+  vp.out = out;
+  vp.partial = h->partial;
+  vp.counters = h->counters;
+  vp.status = h->status;
+  vp.ldo = ldo;
+  vp.N = h->N;
+  vp.M = M;
+  vp.S = p.S;
+  vp.spc = p.spc;
+  vp.wait_limit_ns = h->wait_limit_ns;
+  VerifyLaunch vl;
+  vl.fmt = h->fmt;
+  vl.f16_ops = f16;
+  vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
+  vl.ctas = p.n_tiles * p.S;
+  vl.stream = st;
+  e = h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return QMM_OK;
+}
+
+int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_host, int64_t ldo,
+                    int M, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
+  if (!act_host || !out_host) return QMM_ERR_INVALID_ARG;
+  if (lda < h->K || ldo < h->N) return QMM_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpy2DAsync(h->stage_act, (size_t)h->stage_act_pitch * 2, act_host,
+                                    (size_t)lda * 2, (size_t)h->K * 2, (size_t)M,
+                                    cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int rc = qmm_verify(h, h->stage_act, h->stage_act_pitch, h->stage_out, h->N, M, stream);
+  if (rc != QMM_OK) return rc;
+  e = cudaMemcpy2DAsync(out_host, (size_t)ldo * 4, h->stage_out, (size_t)h->N * 4, (size_t)h->N * 4,
+                        (size_t)M, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return QMM_OK;
+}
+
+int qmm_sync_status(qmm_t h, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int word = 0;
+  e = cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (word != 0) {
+    // A kernel gave up: its split counters may be half-counted.  Reset.
+    cudaMemset(h->status, 0, sizeof(int));
+    cudaMemset(h->counters, 0, (size_t)h->plan.n_tiles * sizeof(int));
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    return QMM_ERR_TIMEOUT;
+  }
+  return QMM_OK;
+}
+
+int qmm_last_cuda_error(qmm_t h) {
+  if (!h) return g_last_error.load();
+  if (!is_live(h)) return QMM_ERR_STATE;
+  return h->last_cuda_error;
+}
+
+int qmm_get_info(qmm_t h, qmm_info* info) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (!info || info->struct_size != sizeof(qmm_info)) return QMM_ERR_INVALID_ARG;
+  const Plan& p = h->plan;
+  info->format = (uint32_t)h->fmt;
+  info->flags = h->flags;
+  info->N = h->N;
+  info->K = h->K;
+  info->weight_bytes = h->fmt == 0 ? h->N * h->K / 32 * 18
+                                   : h->N * h->K + 4 * (h->N / 128) * (h->K / 128);
+  info->device_weight_bytes = (int64_t)h->wdev_bytes;
+  info->scratch_bytes = (int64_t)(h->act_bytes + h->partial_bytes + MAX_M * p.S * sizeof(float) +
+                                  p.n_tiles * sizeof(int) + sizeof(int));
+  info->n_tiles = p.n_tiles;
+  info->k_splits = p.S;
+  info->ctas = p.n_tiles * p.S;
+  info->stages_per_cta = p.spc;
+  info->stage_bytes = p.stage_bytes;
+  info->pipeline_depth = p.depth;
+  info->device = h->device;
+  info->sm_count = h->sm_count;
+  return QMM_OK;
+}
+
+int qmm_dequantize(qmm_t h, float* w_out, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (!w_out) return QMM_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  const Plan& p = h->plan;
+  cudaError_t e = launch_dequant(h->fmt, h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
+                                 (cudaStream_t)stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(h, e);
+}
+
+int qmm_hadamard32(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K, void* stream) {
+  if (!act || !act_out) return QMM_ERR_INVALID_ARG;
+  if (M < 1) return QMM_ERR_M_RANGE;
+  if (K < 32 || K % 32) return QMM_ERR_SHAPE;
+  if (((uintptr_t)act & 15) || ((uintptr_t)act_out & 15) || lda < K || (lda & 7)) return QMM_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  int rc = check_device(&dev, &sms);
+  if (rc != QMM_OK) return rc;
+  cudaError_t e = launch_hadamard32(act, lda, act_out, M, K, sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
+}
+
+int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
+                      void* stream) {
+  if (!w || !blocks) return QMM_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)QMM_FLAG_HADAMARD32) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32) return QMM_ERR_SHAPE;
+  if ((uintptr_t)w & 15) return QMM_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  int rc = check_device(&dev, &sms);
+  if (rc != QMM_OK) return rc;
+  cudaError_t e = launch_quantize_q4(w, N, K, (flags & QMM_FLAG_HADAMARD32) ? 1 : 0, blocks,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
+}
+
+int qmm_quantize_fp8(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* codes,
+                     float* scales, void* stream) {
+  if (!w || !codes || !scales) return QMM_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)QMM_FLAG_HADAMARD32) return QMM_ERR_INVALID_ARG;
+  if (N < 128 || K < 128 || N % 128 || K % 128) return QMM_ERR_SHAPE;
+  if (((uintptr_t)w & 15) || ((uintptr_t)codes & 15)) return QMM_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  int rc = check_device(&dev, &sms);
+  if (rc != QMM_OK) return rc;
+  cudaError_t e = launch_quantize_fp8(w, N, K, (flags & QMM_FLAG_HADAMARD32) ? 1 : 0, codes, scales,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
+}
+
+int qmm_debug_set_wait_limit(qmm_t h, int64_t ns) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (ns < 0) return QMM_ERR_INVALID_ARG;
+  h->wait_limit_ns = (uint64_t)ns;
+  return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,535 @@
+// qmm_aux.cu -- activation pre-pass, Walsh-Hadamard rotation, weight repack,
+// exact dequantization hook and the device quantizers (the offline tools that
+// write Q4_0 / FP8 weight files, including the rotated "-H32" variant).
+#include <cuda_runtime.h>
+
+#include "qmm_common.cuh"
+#include "qmm_kernels.h"
+
+namespace qmm {
+
+// ---------------------------------------------------------------------------
+// 32-point Walsh-Hadamard rotation across 8 lanes holding 4 consecutive values
+// each: strides 1 and 2 inside the lane, then strides 4, 8 and 16 with lane
+// shuffles (partner lane = lane ^ 1, ^ 2, ^ 4).  Every stage maps the pair
+// (x at the lower index, y at the upper) to (x + y, x - y) in fp32, which is
+// the stage order and arithmetic of the unnormalised transform
+// ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve, and 4-bit activations
+// with a Hadamard rotation", section "Prompt processing: 4-bit activations,
+// rotated first": two in-register butterfly steps and three lane shuffles].
+// All 32 lanes of the warp must call it (groups of 8 lanes = 4 blocks).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fwht32_lanes(float (&v)[4], int lane) {
+  float x, y;
+  // stride 1: (0,1), (2,3)
+  x = v[0]; y = v[1]; v[0] = __fadd_rn(x, y); v[1] = __fsub_rn(x, y);
+  x = v[2]; y = v[3]; v[2] = __fadd_rn(x, y); v[3] = __fsub_rn(x, y);
+  // stride 2: (0,2), (1,3)
+  x = v[0]; y = v[2]; v[0] = __fadd_rn(x, y); v[2] = __fsub_rn(x, y);
+  x = v[1]; y = v[3]; v[1] = __fadd_rn(x, y); v[3] = __fsub_rn(x, y);
+  // strides 4, 8, 16 across lanes
+#pragma unroll
+  for (int d = 1; d <= 4; d <<= 1) {
+    const bool upper = (lane & d) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float other = __shfl_xor_sync(0xFFFFFFFFu, v[e], d);
+      v[e] = upper ? __fsub_rn(other, v[e]) : __fadd_rn(v[e], other);
+    }
+  }
+}
+
+__device__ __forceinline__ void load4_bf16(const uint16_t* p, float (&v)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float((raw.x & 0xFFFFu) << 16);
+  v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+  v[2] = __uint_as_float((raw.y & 0xFFFFu) << 16);
+  v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+}
+
+// ---------------------------------------------------------------------------
+// Activation pre-pass.  CTA (s, m) converts row m's K range of split s into the
+// stage-ordered 16-bit scratch read by the verify kernel.
+//   OUT_F16 = false: bf16 copied unchanged (exact); multiplier 1.
+//   OUT_F16 = true : values (rotated when HAD) are multiplied by 2^e with e
+//                    chosen so that the largest magnitude of the range lands
+//                    in [2^14, 2^15), rounded to f16, and 2^-e is recorded as
+//                    the multiplier of this (row, split)'s partial sums.
+// Elements past K are written as zeros.
+// ---------------------------------------------------------------------------
+template <bool OUT_F16, bool HAD>
+__global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ PrepParams p) {
+  pdl_trigger();
+  const int s = blockIdx.x, m = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t k0 = (int64_t)s * p.spc * p.stage_k;
+  const int64_t kr = (int64_t)p.spc * p.stage_k;  // elements of this split
+  const int pitch = p.stage_k + 8;
+  const uint16_t* src = p.act + (int64_t)m * p.lda;
+  // Earlier kernels may still read the scratch this writes.
+  pdl_wait();
+
+  auto dst_index = [&](int64_t kl) -> int64_t {
+    const int64_t st = (int64_t)s * p.spc + kl / p.stage_k;
+    return (st * MAX_M + m) * pitch + (kl % p.stage_k);
+  };
+
+  if constexpr (!OUT_F16) {
+    for (int64_t kl = (int64_t)tid * 4; kl < kr; kl += 256 * 4) {
+      const int64_t k = k0 + kl;
+      uint2 v = make_uint2(0, 0);
+      if (k < p.K) v = *reinterpret_cast<const uint2*>(src + k);  // K % 32 == 0: whole group in range
+      *reinterpret_cast<uint2*>(p.out + dst_index(kl)) = v;
+    }
+    if (tid == 0) p.out_scale[m * p.S + s] = 1.0f;
+    return;
+  } else {
+    __shared__ float s_max[8];
+    __shared__ float s_mul;
+    // pass 1: largest magnitude of the (rotated) values
+    float amax = 0.f;
+    for (int64_t base = (int64_t)(tid & ~31) * 4; base < kr; base += 256 * 4) {
+      const int64_t kl = base + lane * 4;
+      const int64_t k = k0 + kl;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (k < p.K) load4_bf16(src + k, v);
+      if constexpr (HAD) fwht32_lanes(v, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[e]));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+    if (lane == 0) s_max[tid >> 5] = amax;
+    __syncthreads();
+    if (tid == 0) {
+      float a = s_max[0];
+      for (int w = 1; w < 8; ++w) a = fmaxf(a, s_max[w]);
+      int sh = 0;
+      if (a > 0.f && isfinite(a)) {
+        int E;
+        frexpf(a, &E);  // a = f * 2^E, f in [0.5, 1)
+        sh = 15 - E;    // a * 2^sh in [2^14, 2^15)
+        sh = sh > 100 ? 100 : (sh < -100 ? -100 : sh);
+      }
+      s_mul = ldexpf(1.0f, sh);
+      p.out_scale[m * p.S + s] = ldexpf(1.0f, -sh);
+    }
+    __syncthreads();
+    const float mul = s_mul;
+    // pass 2: scale (exact power of two), round to f16, store
+    for (int64_t base = (int64_t)(tid & ~31) * 4; base < kr; base += 256 * 4) {
+      const int64_t kl = base + lane * 4;
+      const int64_t k = k0 + kl;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (k < p.K) load4_bf16(src + k, v);
+      if constexpr (HAD) fwht32_lanes(v, lane);
+      const __half2 h01 = __floats2half2_rn(v[0] * mul, v[1] * mul);
+      const __half2 h23 = __floats2half2_rn(v[2] * mul, v[3] * mul);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&h01);
+      o.y = *reinterpret_cast<const uint32_t*>(&h23);
+      *reinterpret_cast<uint2*>(p.out + dst_index(kl)) = o;
+    }
+  }
+}
+
+// Standalone rotation: fp32 output [M][K], each warp rotates 4 blocks at a time.
+__global__ void __launch_bounds__(256) hadamard32_kernel(const uint16_t* __restrict__ act, int64_t lda,
+                                                         float* __restrict__ out, int M, int64_t K) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  const int64_t per_row = K / 128 + ((K % 128) ? 1 : 0);  // 128-element groups per row
+  for (int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); wid < per_row * M; wid += warps) {
+    const int m = (int)(wid / per_row);
+    const int64_t k = (wid % per_row) * 128 + lane * 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool ok = k < K;  // K % 32 == 0: an 8-lane group is all in or all out
+    if (ok) load4_bf16(act + (int64_t)m * lda + k, v);
+    fwht32_lanes(v, lane);
+    if (ok) *reinterpret_cast<float4*>(out + (int64_t)m * K + k) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Repack: canonical Q4_0 blocks -> tile-major stage stream (see qmm_common.cuh).
+// One thread per (unit, lane).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t q4_code(const uint8_t* blocks, int64_t N, int64_t K, int64_t n,
+                                            int64_t k) {
+  if (n >= N || k >= K) return 8u;
+  const uint8_t* blk = blocks + (n * (K / 32) + k / 32) * 18;
+  const int e = (int)(k % 32);
+  const uint8_t byte = blk[2 + (e & 15)];
+  return (e < 16) ? (byte & 15u) : (byte >> 4);
+}
+
+__device__ __forceinline__ uint16_t q4_scale_bits(const uint8_t* blocks, int64_t N, int64_t K,
+                                                  int64_t n, int64_t b) {
+  if (n >= N || b * 32 >= K) return 0;
+  const uint8_t* blk = blocks + (n * (K / 32) + b) * 18;
+  return (uint16_t)(blk[0] | (blk[1] << 8));
+}
+
+__global__ void repack_q4_kernel(const uint8_t* __restrict__ blocks, int64_t N, int64_t K, int S,
+                                 int spc, int64_t total_units, uint8_t* __restrict__ wdev) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int64_t stage_global = u;  // ((tile * S + split) * spc + i)
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t kstage = ((int64_t)split * spc + i) * Q4_STAGE_K + 64 * c;
+  uint32_t words[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int blk = v >> 1, j = v & 1;
+    uint32_t w = 0;
+#pragma unroll
+    for (int pn = 0; pn < 8; ++pn) {
+      const int pair = pn & 3, half = pn >> 2;
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (pair & 1);
+      const int64_t k = kstage + 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);
+      w |= q4_code(blocks, N, K, n, k) << (4 * pn);
+    }
+    words[v] = w;
+  }
+  uint8_t* unit = wdev + stage_global * Q4_STAGE_BYTES + (int64_t)(c * 8 + r) * Q4_UNIT_BYTES;
+  *reinterpret_cast<uint4*>(unit + 16 * lane) = make_uint4(words[0], words[1], words[2], words[3]);
+  if (t == 0) {
+    const int64_t n = tile * TILE_N + 16 * r + g;
+    const int64_t b0 = kstage / 32;
+    uint2 sc;
+    sc.x = (uint32_t)q4_scale_bits(blocks, N, K, n, b0) |
+           ((uint32_t)q4_scale_bits(blocks, N, K, n + 8, b0) << 16);
+    sc.y = (uint32_t)q4_scale_bits(blocks, N, K, n, b0 + 1) |
+           ((uint32_t)q4_scale_bits(blocks, N, K, n + 8, b0 + 1) << 16);
+    *reinterpret_cast<uint2*>(unit + 512 + 8 * g) = sc;
+  }
+}
+
+__global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                                  int64_t N, int64_t K, int S, int spc, int64_t total_units,
+                                  uint8_t* __restrict__ wdev) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int64_t stage_global = u;
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t kt = (int64_t)split * spc + i;  // 128-column tile index
+  const int64_t kbase = kt * F8_STAGE_K + 32 * c;
+  uint32_t words[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int j = v >> 1, h = v & 1;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int a = 2 * h + (e >> 1);
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (a & 1);
+      const int64_t k = kbase + 16 * j + 2 * t + (e & 1) + 8 * (a >> 1);
+      const uint32_t code = (n < N && k < K) ? codes[n * K + k] : 0u;
+      w |= code << (8 * e);
+    }
+    words[v] = w;
+  }
+  uint8_t* stage = wdev + stage_global * F8_STAGE_BYTES;
+  uint8_t* unit = stage + (int64_t)(c * 8 + r) * F8_UNIT_BYTES;
+  *reinterpret_cast<uint4*>(unit + 16 * lane) = make_uint4(words[0], words[1], words[2], words[3]);
+  if (c == 0 && r == 0 && lane == 0) {
+    const int64_t tk_n = K / 128;
+    float s = 0.f;
+    if (tile * TILE_N < N && kt * 128 < K) s = scales[tile * tk_n + kt];
+    *reinterpret_cast<float4*>(stage + CONSUMER_WARPS * 8 * F8_UNIT_BYTES) = make_float4(s, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exact dequantization from the repacked stream (test hook): one thread per
+// (unit, lane) decodes its 16 bytes back to (n, k) positions.
+// ---------------------------------------------------------------------------
+__global__ void dequant_q4_kernel(const uint8_t* __restrict__ wdev, int64_t N, int64_t K, int S, int spc,
+                                  int64_t total_units, float* __restrict__ out) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int64_t stage_global = u;
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t kstage = ((int64_t)split * spc + i) * Q4_STAGE_K + 64 * c;
+  const uint8_t* unit = wdev + stage_global * Q4_STAGE_BYTES + (int64_t)(c * 8 + r) * Q4_UNIT_BYTES;
+  const uint4 cw = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+  const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
+  const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int blk = v >> 1, j = v & 1;
+    const uint32_t dp = blk ? sc.y : sc.x;
+#pragma unroll
+    for (int pn = 0; pn < 8; ++pn) {
+      const int pair = pn & 3, half = pn >> 2;
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (pair & 1);
+      const int64_t k = kstage + 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);
+      if (n < N && k < K) {
+        const uint16_t dbits = (uint16_t)((pair & 1) ? (dp >> 16) : (dp & 0xFFFF));
+        const int q = (int)((words[v] >> (4 * pn)) & 15u);
+        out[n * K + k] = __half2float(__ushort_as_half(dbits)) * (float)(q - 8);
+      }
+    }
+  }
+}
+
+__global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, int64_t N, int64_t K, int S, int spc,
+                                   int64_t total_units, float* __restrict__ out) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int64_t stage_global = u;
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t kbase = ((int64_t)split * spc + i) * F8_STAGE_K + 32 * c;
+  const uint8_t* stage = wdev + stage_global * F8_STAGE_BYTES;
+  const uint8_t* unit = stage + (int64_t)(c * 8 + r) * F8_UNIT_BYTES;
+  const float s = *reinterpret_cast<const float*>(stage + CONSUMER_WARPS * 8 * F8_UNIT_BYTES);
+  const uint4 cw = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+  const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int j = v >> 1, h = v & 1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int a = 2 * h + (e >> 1);
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (a & 1);
+      const int64_t k = kbase + 16 * j + 2 * t + (e & 1) + 8 * (a >> 1);
+      if (n < N && k < K) {
+        const uint32_t code = (words[v] >> (8 * e)) & 0xFFu;
+        uint32_t h2;
+        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+            : "=r"(h2)
+            : "r"(code));
+        const float w = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+        out[n * K + k] = __fmul_rn(w, s);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Quantizers (offline tools).
+// ---------------------------------------------------------------------------
+// Rotate a 32-block held by one thread (same stage order as fwht32_lanes).
+__device__ __forceinline__ void fwht32_thread(float (&v)[32]) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i & h) continue;
+      const float x = v[i], y = v[i + h];
+      v[i] = __fadd_rn(x, y);
+      v[i + h] = __fsub_rn(x, y);
+    }
+  }
+}
+
+__global__ void quantize_q4_kernel(const float* __restrict__ w, int64_t N, int64_t K, int had,
+                                   uint8_t* __restrict__ blocks) {
+  const int64_t nb = K / 32;
+  const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (id >= N * nb) return;
+  const int64_t n = id / nb, b = id % nb;
+  float x[32];
+  const float4* src = reinterpret_cast<const float4*>(w + n * K + 32 * b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = src[i];
+    x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+  }
+  if (had) {
+    fwht32_thread(x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], 0.03125f);
+  }
+  float amax = 0.f, amax_s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = fabsf(x[i]);
+    if (a > amax) { amax = a; amax_s = x[i]; }
+  }
+  const float d32 = __fdiv_rn(amax_s, -8.0f);
+  const float inv = (d32 != 0.f) ? __fdiv_rn(1.0f, d32) : 0.f;
+  uint8_t q[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    int qi = (int)roundf(__fmul_rn(x[i], inv)) + 8;
+    qi = qi < 0 ? 0 : (qi > 15 ? 15 : qi);
+    q[i] = (uint8_t)qi;
+  }
+  const uint16_t d16 = __half_as_ushort(__float2half_rn(d32));
+  uint8_t* dst = blocks + id * 18;
+  dst[0] = (uint8_t)(d16 & 0xFF);
+  dst[1] = (uint8_t)(d16 >> 8);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) dst[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+// One CTA per 128x128 tile.  Pass 1: max |value| (after the optional rotation);
+// pass 2: codes.  Each thread owns whole 32-blocks (row n, block b).
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const float* __restrict__ w, int64_t N, int64_t K,
+                                                           int had, uint8_t* __restrict__ codes,
+                                                           float* __restrict__ scales) {
+  const int64_t tn = blockIdx.y, tk = blockIdx.x;
+  const int tid = threadIdx.x;
+  __shared__ float s_red[8];
+  __shared__ float s_s;
+  auto load_block = [&](int idx, float (&x)[32]) {
+    const int64_t n = tn * 128 + idx / 4;
+    const int64_t k = tk * 128 + 32 * (idx % 4);
+    const float4* src = reinterpret_cast<const float4*>(w + n * K + k);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = src[i];
+      x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+    }
+    if (had) {
+      fwht32_thread(x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], 0.03125f);
+    }
+  };
+  float amax = 0.f;
+  for (int idx = tid; idx < 512; idx += 256) {
+    float x[32];
+    load_block(idx, x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+  if ((tid & 31) == 0) s_red[tid >> 5] = amax;
+  __syncthreads();
+  if (tid == 0) {
+    float a = s_red[0];
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, s_red[i]);
+    const float s = __fdiv_rn(a, 448.0f);
+    s_s = s;
+    scales[tn * (K / 128) + tk] = s;
+  }
+  __syncthreads();
+  const float s = s_s;
+  for (int idx = tid; idx < 512; idx += 256) {
+    float x[32];
+    load_block(idx, x);
+    const int64_t n = tn * 128 + idx / 4;
+    const int64_t k = tk * 128 + 32 * (idx % 4);
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        uint16_t pr = 0;
+        if (s != 0.f) {
+          const float lo = __fdiv_rn(x[4 * i + e], s), hi = __fdiv_rn(x[4 * i + e + 1], s);
+          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pr) : "f"(hi), "f"(lo));
+        }
+        word |= (uint32_t)pr << (8 * e);
+      }
+      out[i] = word;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(codes + n * K + k);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+// ---------------------------------------------------------------------------
+cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.M, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!out_f16) return cudaLaunchKernelEx(&cfg, act_prep_kernel<false, false>, p);
+  if (had) return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, true>, p);
+  return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, false>, p);
+}
+
+cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int M, int64_t K,
+                              int sm_count, cudaStream_t st) {
+  const int64_t work = (K / 128 + 1) * M;
+  int64_t blocks = (work + 7) / 8;
+  const int64_t cap = (int64_t)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  hadamard32_kernel<<<(unsigned)blocks, 256, 0, st>>>(act, lda, out, M, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
+                          int n_tiles, int S, int spc, uint8_t* wdev, cudaStream_t st) {
+  const int64_t units = (int64_t)n_tiles * S * spc * CONSUMER_WARPS * 8;
+  const int64_t threads = units * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (fmt == 0)
+    repack_q4_kernel<<<blocks, 256, 0, st>>>(wsrc, N, K, S, spc, units, wdev);
+  else
+    repack_fp8_kernel<<<blocks, 256, 0, st>>>(wsrc, scales, N, K, S, spc, units, wdev);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(int fmt, const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S,
+                           int spc, float* out, cudaStream_t st) {
+  const int64_t units = (int64_t)n_tiles * S * spc * CONSUMER_WARPS * 8;
+  const int64_t threads = units * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (fmt == 0)
+    dequant_q4_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
+  else
+    dequant_fp8_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q4(const float* w, int64_t N, int64_t K, int had, uint8_t* blocks,
+                               cudaStream_t st) {
+  const int64_t n = N * (K / 32);
+  if (n == 0) return cudaSuccess;
+  quantize_q4_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(w, N, K, had, blocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8(const float* w, int64_t N, int64_t K, int had, uint8_t* codes,
+                                float* scales, cudaStream_t st) {
+  dim3 grid((unsigned)(K / 128), (unsigned)(N / 128), 1);
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  quantize_fp8_kernel<<<grid, 256, 0, st>>>(w, N, K, had, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

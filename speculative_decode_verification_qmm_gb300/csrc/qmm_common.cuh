@@ -1,0 +1,290 @@
+// qmm_common.cuh -- layouts, launch parameters and inline-PTX helpers shared by
+// the verify kernels, the activation pre-pass and the tool kernels.
+//
+// Device layout of a repacked weight matrix ("tile-major stage stream").
+//   The N rows are cut into row tiles of TILE_N = 128 rows (zero-padded at the
+//   end) and the K axis into pipeline stages of STAGE_K elements (zero-padded).
+//   The stages of row tile `tile` are split into `S` contiguous K ranges (the
+//   K splits); CTA (tile, s) streams stages [s*spc, (s+1)*spc) where spc is the
+//   number of stages per CTA.  Every stage of every CTA is one contiguous byte
+//   range, so one bulk copy moves it into shared memory:
+//       wdev + ((tile * S + s) * spc + i) * stage_bytes
+//   Inside a stage the bytes are ordered [warp chunk c][row subtile r][unit],
+//   where a unit is what one warp needs for 16 rows x (STAGE_K / 4) columns,
+//   already permuted into mma.sync m16n8k16 A-fragment order: lane l (group
+//   g = l / 4, thread t = l % 4) finds its 16 bytes at unit + 16 l.
+//
+//   Q4_0 (STAGE_K = 256, chunk = 64 columns = two 32-blocks):
+//     unit = 512 B codes + 64 B scales = 576 B.  Lane word v (0..3) covers
+//     block b = v / 2 and k16 step j = v % 2; its nibble p (0..7), with
+//     pair = p & 3 and half = p >> 2, is the element
+//       row = g + 8 * (pair & 1),   k = 32 b + 16 j + 2 t + half + 8 * (pair >> 1)
+//     (pairs 0..3 are the A registers a0..a3).  Nibble pair (p, p + 4) sits in the
+//     low nibbles of the two 16-bit lanes after a right shift by 4 p, which is
+//     exactly the (low, high) element order of one bf16x2 / f16x2 A register.
+//     Scales: for g = 0..7, 8 bytes = fp16 d[g][b0], d[g+8][b0], d[g][b1], d[g+8][b1].
+//   FP8 (STAGE_K = 128, chunk = 32 columns):
+//     unit = 512 B codes; lane word v covers k16 step j = v / 2, half h = v % 2;
+//     byte e (0..3) is element row = g + 8 * ((2h + e/2) & 1),
+//     k = 16 j + 2 t + (e & 1) + 8 * ((2h + e/2) >> 1).  The stage ends with a
+//     16-byte record holding the fp32 scale of its 128x128 tile.
+//
+// Activation scratch: the pre-pass writes the (optionally rotated) activation
+// rows as 16-bit values in the same stage order, [stage][16 rows][ACT_PITCH],
+// with ACT_PITCH = STAGE_K + 8 so that ldmatrix rows fall in distinct banks.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace qmm {
+
+constexpr int TILE_N = 128;           // rows of W per CTA tile
+constexpr int CONSUMER_WARPS = 4;     // warps that compute
+constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;  // + one producer warp
+constexpr int MAX_M = 16;
+
+// Q4_0
+constexpr int Q4_STAGE_K = 256;
+constexpr int Q4_UNIT_BYTES = 576;
+constexpr int Q4_STAGE_BYTES = CONSUMER_WARPS * 8 * Q4_UNIT_BYTES;  // 18432
+// FP8
+constexpr int F8_STAGE_K = 128;
+constexpr int F8_UNIT_BYTES = 512;
+constexpr int F8_STAGE_BYTES = CONSUMER_WARPS * 8 * F8_UNIT_BYTES + 16;  // 16400
+
+__host__ __device__ constexpr int act_pitch(int stage_k) { return stage_k + 8; }
+__host__ __device__ constexpr int act_stage_bytes(int stage_k) {
+  return MAX_M * act_pitch(stage_k) * 2;
+}
+
+// Device error word bits (OR-ed into the handle's status word).
+constexpr int DEV_ERR_TIMEOUT_FULL = 1;   // consumer gave up waiting for a stage
+constexpr int DEV_ERR_TIMEOUT_EMPTY = 2;  // producer gave up waiting for a free slot
+constexpr int DEV_ERR_TIMEOUT_DRAIN = 4;  // copies in flight did not land in time
+
+struct VerifyParams {
+  const uint8_t* wdev;       // repacked weights
+  const uint8_t* act;        // activation scratch (16-bit values, stage order)
+  const float* out_scale;    // [MAX_M][S]: multiplier of split s's partial for row m
+  float* out;                // [M][ldo]
+  float* partial;            // [n_tiles][S][MAX_M][TILE_N]
+  int* counters;             // [n_tiles], zero between launches
+  int* status;               // device error word
+  int64_t ldo;
+  int64_t N;
+  int M;
+  int S;                     // K splits
+  int spc;                   // stages per CTA
+  uint64_t wait_limit_ns;    // bounded waits give up after this (0: at once)
+};
+
+struct PrepParams {
+  const uint16_t* act;       // caller's bf16 rows
+  int64_t lda;
+  uint16_t* out;             // activation scratch
+  float* out_scale;          // [MAX_M][S]
+  int64_t K;                 // true K
+  int M;
+  int S;
+  int spc;
+  int stage_k;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `parity` of barrier `bar`; give up after
+// `limit_ns` nanoseconds (limit 0: give up at once).  Returns true on success.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// One-dimensional bulk copy global -> shared, completing on `bar`'s tx count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Same with an L2 eviction-priority hint (weights stream once: evict first).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Programmatic dependent launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Operand-type traits: mma.sync m16n8k16 with fp32 accumulation, and the
+// exact conversion of a 4-bit code pair (two nibbles in the low nibbles of the
+// two 16-bit lanes) to (q - 8) in that type.
+struct Bf16Op {
+  __device__ __forceinline__ static void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1,
+                                             const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+  }
+  // 4 pairs from one 32-bit word of 8 nibbles: pair p from nibbles (p, p + 4).
+  // bf16 128.0 = 0x4300 has a 7-bit mantissa whose low 4 bits take q exactly;
+  // subtracting 136 = 0x4308 leaves q - 8.
+  __device__ __forceinline__ static void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+    const uint32_t magic = 0x43004300u, bias = 0x43084308u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      uint32_t x;
+      asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x) : "r"(w >> (4 * p)), "r"(0x000F000Fu), "r"(magic));
+      asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r[p]) : "r"(x), "r"(bias));
+    }
+  }
+};
+
+struct F16Op {
+  __device__ __forceinline__ static void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1,
+                                             const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+  }
+  // f16 1024.0 = 0x6400 has a 10-bit mantissa: nibbles at bit offsets 0 and 4
+  // of each lane are taken in place (1024 + q and 1024 + 16 q), the other two
+  // after one shift by 8.  (1024 + q) - 1032 and (1024 + 16 q) / 16 - 72 are
+  // both q - 8, exactly.
+  __device__ __forceinline__ static void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+    const uint32_t magic = 0x64006400u;
+    const uint32_t bias_lo = 0x64086408u;   // 1032
+    const uint32_t sixteenth = 0x2C002C00u; // 1/16
+    const uint32_t bias_hi = 0xD480D480u;   // -72
+    const uint32_t w8 = w >> 8;
+    uint32_t x0, x1, x2, x3;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x0) : "r"(w), "r"(0x000F000Fu), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x1) : "r"(w), "r"(0x00F000F0u), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x2) : "r"(w8), "r"(0x000F000Fu), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(x3) : "r"(w8), "r"(0x00F000F0u), "r"(magic));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(x0), "r"(bias_lo));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[1]) : "r"(x1), "r"(sixteenth), "r"(bias_hi));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[2]) : "r"(x2), "r"(bias_lo));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[3]) : "r"(x3), "r"(sixteenth), "r"(bias_hi));
+  }
+};
+
+// acc[0..1] += d * p[0..1] as one packed fp32x2 FMA (two IEEE fma.rn).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float d, float p0, float p1) {
+  float2 r = __ffma2_rn(make_float2(d, d), make_float2(p0, p1), make_float2(a0, a1));
+  a0 = r.x;
+  a1 = r.y;
+}
+
+}  // namespace qmm

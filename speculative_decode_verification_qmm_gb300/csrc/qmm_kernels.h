@@ -1,0 +1,44 @@
+// qmm_kernels.h -- host launchers of the library's kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm_common.cuh"
+
+namespace qmm {
+
+// Verify kernel configuration chosen by the host for one launch.
+struct VerifyLaunch {
+  int fmt;        // 0 Q4_0, 1 FP8
+  bool f16_ops;   // Q4_0: f16 operands (Hadamard path) instead of bf16
+  bool simt;      // CUDA-core baseline (Q4_0 only)
+  int ctas;
+  cudaStream_t stream;
+};
+
+// Pipeline depth (stages in flight per CTA), dynamic shared memory, and the
+// kernels' shared-memory attribute (set on the current device).
+int q4_pipeline_depth();
+int fp8_pipeline_depth();
+size_t q4_smem_bytes();
+size_t fp8_smem_bytes();
+cudaError_t prepare_q4_attributes();
+cudaError_t prepare_fp8_attributes();
+
+cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l);
+cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l);
+
+cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStream_t st);
+cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int M, int64_t K,
+                              int sm_count, cudaStream_t st);
+cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
+                          int n_tiles, int S, int spc, uint8_t* wdev, cudaStream_t st);
+cudaError_t launch_dequant(int fmt, const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S,
+                           int spc, float* out, cudaStream_t st);
+cudaError_t launch_quantize_q4(const float* w, int64_t N, int64_t K, int had, uint8_t* blocks,
+                               cudaStream_t st);
+cudaError_t launch_quantize_fp8(const float* w, int64_t N, int64_t K, int had, uint8_t* codes,
+                                float* scales, cudaStream_t st);
+
+}  // namespace qmm

@@ -1,0 +1,58 @@
+// qmm_verify_q4.cu -- Q4_0 instantiations of the verify kernel and their launcher.
+#include "qmm_kernels.h"
+#include "qmm_verify.cuh"
+
+namespace qmm {
+
+namespace {
+constexpr int NS_Q4 = 3;
+
+template <typename Op, int NT8, bool SIMT>
+cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)l.ctas, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4>::BYTES;
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_kernel<0, Op, NT8, SIMT, NS_Q4>, p);
+}
+
+template <typename Op, int NT8, bool SIMT>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(verify_kernel<0, Op, NT8, SIMT, NS_Q4>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SmemLayout<0, NS_Q4>::BYTES);
+}
+}  // namespace
+
+cudaError_t prepare_q4_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<Bf16Op, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<Bf16Op, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<F16Op, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<F16Op, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<Bf16Op, 1, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<Bf16Op, 2, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<F16Op, 1, true>()) != cudaSuccess) return e;
+  return set_attr<F16Op, 2, true>();
+}
+
+size_t q4_smem_bytes() { return SmemLayout<0, NS_Q4>::BYTES; }
+int q4_pipeline_depth() { return NS_Q4; }
+
+cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l) {
+  const bool nt2 = p.M > 8;
+  if (l.simt) {
+    if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, true>(p, l) : launch_one<F16Op, 1, true>(p, l);
+    return nt2 ? launch_one<Bf16Op, 2, true>(p, l) : launch_one<Bf16Op, 1, true>(p, l);
+  }
+  if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, false>(p, l) : launch_one<F16Op, 1, false>(p, l);
+  return nt2 ? launch_one<Bf16Op, 2, false>(p, l) : launch_one<Bf16Op, 1, false>(p, l);
+}
+
+}  // namespace qmm
