@@ -351,6 +351,16 @@ __device__ __forceinline__ void fwht32_thread(float (&v)[32]) {
   }
 }
 
+// Round half away from zero, from the definition: t = r + f with r = trunc(t)
+// and f = t - r exact (|t| < 2^23); step away from zero when |f| >= 1/2.
+__device__ __forceinline__ int round_half_away(float t) {
+  const float r = truncf(t);
+  const float f = __fsub_rn(t, r);
+  int q = (int)r;
+  if (fabsf(f) >= 0.5f) q += (t < 0.f) ? -1 : 1;
+  return q;
+}
+
 __global__ void quantize_q4_kernel(const float* __restrict__ w, int64_t N, int64_t K, int had,
                                    uint8_t* __restrict__ blocks) {
   const int64_t nb = K / 32;
@@ -380,16 +390,21 @@ __global__ void quantize_q4_kernel(const float* __restrict__ w, int64_t N, int64
   uint8_t q[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    int qi = (int)roundf(__fmul_rn(x[i], inv)) + 8;
+    int qi = round_half_away(__fmul_rn(x[i], inv)) + 8;
     qi = qi < 0 ? 0 : (qi > 15 ? 15 : qi);
     q[i] = (uint8_t)qi;
   }
-  const uint16_t d16 = __half_as_ushort(__float2half_rn(d32));
-  uint8_t* dst = blocks + id * 18;
-  dst[0] = (uint8_t)(d16 & 0xFF);
-  dst[1] = (uint8_t)(d16 >> 8);
+  const unsigned short d16 = __half_as_ushort(__float2half_rn(d32));
+  // 18-byte blocks start on even addresses: write nine aligned 16-bit words
+  // (little endian: fp16 d, then code bytes 2j and 2j+1 of the block).
+  unsigned short* dst = reinterpret_cast<unsigned short*>(blocks + id * 18);
+  dst[0] = d16;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) dst[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+  for (int j = 0; j < 8; ++j) {
+    const unsigned int lo = (unsigned int)q[2 * j] | ((unsigned int)q[2 * j + 16] << 4);
+    const unsigned int hi = (unsigned int)q[2 * j + 1] | ((unsigned int)q[2 * j + 17] << 4);
+    dst[1 + j] = (unsigned short)(lo | (hi << 8));
+  }
 }
 
 // One CTA per 128x128 tile.  Pass 1: max |value| (after the optional rotation);

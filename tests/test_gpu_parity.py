@@ -91,10 +91,19 @@ def test_quantize_q4_bit_exact(hadamard):
     w[1, 32:64] = 0.5
     w[2, 64:96] *= 1e-6
     w[3, 96 + 2], w[3, 96 + 20] = -0.3, 0.3
-    w[4, :32] = np.float32(1e5)  # fp16 scale overflows to infinity
+    w[4, :32] = np.float32(1e5)
+    w[5, :32] = np.float32(6e5)  # the fp16 scale overflows to infinity
     got = q.quantize_q4_0(torch.from_numpy(w).cuda(), hadamard=hadamard).cpu().numpy()
     ref = O.q4_0_quantize_h32(w) if hadamard else O.q4_0_quantize(w)
-    assert (got == ref).all()
+    bad = np.argwhere((got != ref).any(axis=2))
+    detail = []
+    for n, b in bad[:4]:
+        x = w[n, 32 * b:32 * b + 32]
+        dg = np.array([got[n, b, 0] | (got[n, b, 1] << 8)], np.uint16).view(np.float16)[0]
+        dr = np.array([ref[n, b, 0] | (ref[n, b, 1] << 8)], np.uint16).view(np.float16)[0]
+        detail.append(f"block ({n},{b}) gpu {got[n, b].tolist()} (d {float(dg)!r}) oracle "
+                      f"{ref[n, b].tolist()} (d {float(dr)!r}) x {[float(v).hex() for v in x[:4]]}")
+    assert bad.size == 0, f"{len(bad)} blocks differ; " + "; ".join(detail)
 
 
 @pytest.mark.parametrize("hadamard", [False, True])
