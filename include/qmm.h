@@ -157,6 +157,32 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
 int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_host,
                     int64_t ldo, int M, void* stream);
 
+/* The same product as qmm_verify, for callers that cannot have device memory
+ * allocated for them.  The pages have no counterpart of this call.  Some
+ * callers may not allocate device memory when they run: code captured into a
+ * CUDA graph under the global capture mode (cudaMalloc is refused there), or a
+ * host runtime that owns every device allocation and hands the library only
+ * the buffers it passes.  This call allocates nothing and does not use the
+ * working memory of the handle: its activation scratch, split partials and
+ * split counters live in one fixed array of QMM_NOALLOC_SCRATCH_BYTES bytes
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The handle (created earlier, which does allocate) supplies
+ * the weights and the status word; act and out follow qmm_verify's rules.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the array and it keeps the last call's contents: the
+ *     split counters are cleared on the stream before each launch.  Calls that
+ *     overlap on the GPU (other streams, other threads) race on the array and
+ *     give wrong results; serialise them.
+ *   - Asynchronous on `stream`.
+ * Errors: as qmm_verify, plus QMM_ERR_SHAPE when the handle's plan needs more
+ * working memory than the array holds (every N <= 34816 with K <= 17408
+ * fits under the planner's default split choice). */
+#define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
+                       int M, void* stream);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Wait for `stream`, then read and clear the handle's device error word.

@@ -20,7 +20,7 @@ from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
-    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_host", "qmm_sync_status",
+    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_host", "qmm_verify_noalloc", "qmm_sync_status",
     "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
     "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
     "QmmError", "load",
@@ -104,6 +104,13 @@ def qmm_verify_host(h, act, out, M: int, stream=None) -> None:
     """act: CPU bf16 [M, K] (pinned is fastest); out: CPU fp32 [M, N]; synchronous."""
     _check("qmm_verify_host", load().qmm_verify_host(h, _ptr(act), act.stride(0), _ptr(out),
                                                      out.stride(0), M, _stream_ptr(stream)))
+
+
+def qmm_verify_noalloc(h, act, out, M: int, stream=None) -> None:
+    """As qmm_verify, with the working memory in the library's fixed array
+    (no allocation; calls that overlap on the GPU race)."""
+    _check("qmm_verify_noalloc", load().qmm_verify_noalloc(h, _ptr(act), act.stride(0), _ptr(out),
+                                                           out.stride(0), M, _stream_ptr(stream)))
 
 
 def qmm_sync_status(h, stream=None) -> int:

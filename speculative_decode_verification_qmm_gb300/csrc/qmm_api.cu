@@ -486,3 +486,103 @@ int qmm_debug_set_wait_limit(qmm_t h, int64_t ns) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// qmm_verify_noalloc: the verify product with its working memory taken from a
+// fixed array that lives in this library, instead of from the handle.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t STATIC_SCRATCH_BYTES = QMM_NOALLOC_SCRATCH_BYTES;
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_static_mu;
+void* g_static_addr[MAX_DEVICES] = {};
+
+// Device address of the array on `dev`, looked up once per device with that
+// device current.  Host code must not use the array's name as an address.
+cudaError_t static_scratch_addr(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = p;
+  }
+  *out = reinterpret_cast<unsigned char*>(g_static_addr[dev]);
+  return cudaSuccess;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out,
+                                  int64_t ldo, int M, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
+  if (!act || !out) return QMM_ERR_INVALID_ARG;
+  if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || lda < h->K || (lda & 7) || ldo < h->N)
+    return QMM_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  const Plan& p = h->plan;
+  // Carve the array: activation scratch | row factors | split partials | split counters.
+  const size_t act_off = 0;
+  const size_t scale_off = align256(act_off + h->act_bytes);
+  const size_t part_off = align256(scale_off + (size_t)MAX_M * p.S * sizeof(float));
+  const size_t cnt_off = align256(part_off + h->partial_bytes);
+  const size_t total = cnt_off + (size_t)p.n_tiles * sizeof(int);
+  if (total > STATIC_SCRATCH_BYTES) return QMM_ERR_SHAPE;
+  unsigned char* base = nullptr;
+  cudaError_t e = static_scratch_addr(dev, &base);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  cudaStream_t st = (cudaStream_t)stream;
+  int* counters = reinterpret_cast<int*>(base + cnt_off);
+  // The split counters must start at zero; the array keeps the last call's contents.
+  e = cudaMemsetAsync(counters, 0, (size_t)p.n_tiles * sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+
+  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
+  const bool f16 = had || h->fmt == 1;
+  PrepParams pp;
+  pp.act = act;
+  pp.lda = lda;
+  pp.out = reinterpret_cast<uint16_t*>(base + act_off);
+  pp.out_scale = reinterpret_cast<float*>(base + scale_off);
+  pp.K = h->K;
+  pp.M = M;
+  pp.S = p.S;
+  pp.spc = p.spc;
+  pp.stage_k = p.stage_k;
+  e = launch_act_prep(pp, f16, had, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+
+  VerifyParams vp;
+  vp.wdev = h->wdev;
+  vp.act = base + act_off;
+  vp.out_scale = reinterpret_cast<const float*>(base + scale_off);
+  vp.out = out;
+  vp.partial = reinterpret_cast<float*>(base + part_off);
+  vp.counters = counters;
+  vp.status = h->status;
+  vp.ldo = ldo;
+  vp.N = h->N;
+  vp.M = M;
+  vp.S = p.S;
+  vp.spc = p.spc;
+  vp.wait_limit_ns = h->wait_limit_ns;
+  VerifyLaunch vl;
+  vl.fmt = h->fmt;
+  vl.f16_ops = f16;
+  vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
+  vl.ctas = p.n_tiles * p.S;
+  vl.stream = st;
+  e = h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return QMM_OK;
+}
