@@ -75,7 +75,10 @@ enum {
   QMM_FLAG_HADAMARD32 = 1u << 0,
   /* Use the CUDA-core (FP32 FMA) verify kernel instead of the tensor-core one.
    * Same results within the tolerance; kept as the measured baseline. */
-  QMM_FLAG_SIMT = 1u << 1
+  QMM_FLAG_SIMT = 1u << 1,
+  /* Q4_0 without rotation: use the warp-level mma.sync kernel instead of the
+   * tcgen05 one (same results within the tolerance; kept for comparison). */
+  QMM_FLAG_MMA_SYNC = 1u << 2
 };
 
 /* Description of one weight matrix W[N][K]. */
@@ -94,7 +97,8 @@ typedef struct {
                                 FP8: uint8 E4M3 codes [N][K], row-major.        */
   const float* scales;       /* FP8: fp32 [N/128][K/128] row-major; Q4_0: NULL  */
   int32_t k_splits;          /* 0: the planner chooses; > 0: use this many K splits
-                                (tuning and tests; clamped to the stage count)  */
+                                (tuning and tests; clamped to the stage count
+                                and to 16, the largest cluster)                 */
 } qmm_desc;
 
 /* Opaque handle: owns the device copy of W (repacked for the kernels) and the
@@ -163,22 +167,24 @@ int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_h
  * CUDA graph under the global capture mode (cudaMalloc is refused there), or a
  * host runtime that owns every device allocation and hands the library only
  * the buffers it passes.  This call allocates nothing and does not use the
- * working memory of the handle: its activation scratch, split partials and
- * split counters live in one fixed array of QMM_NOALLOC_SCRATCH_BYTES bytes
- * inside the library, which every GPU that loads the library holds until the
- * process exits.  The handle (created earlier, which does allocate) supplies
- * the weights and the status word; act and out follow qmm_verify's rules.
+ * working memory of the handle: on the paths that need working memory (the
+ * Hadamard rotation and FP8, whose activations go through the pre-pass) the
+ * rotated activation rows and their per-(row, split) factors live in one fixed
+ * array of QMM_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library holds until the process exits; the bf16 Q4_0 path
+ * reads the caller's rows directly and needs none.  The handle (created
+ * earlier, which does allocate) supplies the weights and the status word; act
+ * and out follow qmm_verify's rules.
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream
  *     capture.
- *   - All calls share the array and it keeps the last call's contents: the
- *     split counters are cleared on the stream before each launch.  Calls that
- *     overlap on the GPU (other streams, other threads) race on the array and
- *     give wrong results; serialise them.
+ *   - All calls share the array and it keeps the last call's contents; every
+ *     call rewrites the part it reads before reading it.  Calls that overlap
+ *     on the GPU (other streams, other threads) race on the array and give
+ *     wrong results; serialise them.
  *   - Asynchronous on `stream`.
- * Errors: as qmm_verify, plus QMM_ERR_SHAPE when the handle's plan needs more
- * working memory than the array holds (every N <= 34816 with K <= 17408
- * fits under the planner's default split choice). */
+ * Errors: as qmm_verify, plus QMM_ERR_SHAPE when the handle's rotated or FP8
+ * activations need more than the array holds (K above about 127,000). */
 #define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
 int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
                        int M, void* stream);

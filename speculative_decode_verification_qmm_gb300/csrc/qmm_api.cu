@@ -1,5 +1,7 @@
 // qmm_api.cu -- the C ABI (include/qmm.h): handles, validation, the launch
 // planner, device repack at create time, and the asynchronous verify call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -8,7 +10,7 @@
 #include <mutex>
 #include <unordered_set>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_kernels.h"
 
 using namespace qmm;
@@ -21,13 +23,13 @@ constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 // Planner constants: HBM copy bandwidth of the part and what one CTA with its
 // pipeline full sustains (both only rank candidate plans; see plan()).
 constexpr double PLAN_HBM_BPS = 6.8e12;
-constexpr double PLAN_CTA_BPS = 45e9;
-constexpr double PLAN_FIXUP_S = 0.6e-6;
-constexpr double PLAN_L2_BPS = 10e12;
+constexpr double PLAN_CTA_BPS = 30e9;
+constexpr double PLAN_CLUSTER_REDUCE_S = 0.4e-6;
 
 struct Plan {
   int n_tiles = 0, S = 1, spc = 1, stage_k = 0, stage_bytes = 0, depth = 0;
   int64_t nst = 0;  // stages per row tile before padding
+  bool tc = false;  // tcgen05 kernel and its weight layout
 };
 
 }  // namespace
@@ -45,15 +47,18 @@ struct qmm_handle {
   uint16_t* act_scratch = nullptr;
   size_t act_bytes = 0;
   float* out_scale = nullptr;  // [MAX_M][S]
-  float* partial = nullptr;    // [n_tiles][S][MAX_M][TILE_N]
-  size_t partial_bytes = 0;
-  int* counters = nullptr;     // [n_tiles]
   int* status = nullptr;       // device error word
   uint16_t* stage_act = nullptr;  // host-buffer path: [MAX_M][act_pitch]
   int64_t stage_act_pitch = 0;
   float* stage_out = nullptr;     // [MAX_M][N]
   uint64_t wait_limit_ns = DEFAULT_WAIT_LIMIT_NS;
   int last_cuda_error = 0;
+  // tcgen05 path: tensor map over the last activation rows seen (re-encoded
+  // when the pointer, row stride or M changes)
+  CUtensorMap act_map;
+  const void* map_ptr = nullptr;
+  int64_t map_lda = -1;
+  int map_M = -1;
 };
 
 namespace {
@@ -94,15 +99,16 @@ int cuda_fail(qmm_handle* h, cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Choose the K split count.  Candidates keep every CTA resident in one wave
-// (two CTAs per SM); each is scored by the time to stream its padded bytes at
-// min(HBM bandwidth, CTAs x per-CTA rate) plus a fixed cost and the partial
-// traffic when the splits need the last-CTA reduction.
-Plan make_plan(int fmt, int64_t N, int64_t K, int sm_count, int forced_splits) {
+// Choose the K split count S (= cluster size).  Candidates keep every CTA
+// resident in one wave (two CTAs per SM; for S > 1 as many clusters as the
+// device holds at once); each is scored by the time to stream its padded bytes
+// at min(HBM bandwidth, CTAs x per-CTA rate) plus the cluster reduction.
+Plan make_plan(int fmt, bool tc, int64_t N, int64_t K, int sm_count, int forced_splits) {
   Plan p;
+  p.tc = tc;
   p.stage_k = fmt == 0 ? Q4_STAGE_K : F8_STAGE_K;
   p.stage_bytes = fmt == 0 ? Q4_STAGE_BYTES : F8_STAGE_BYTES;
-  p.depth = fmt == 0 ? q4_pipeline_depth() : fp8_pipeline_depth();
+  p.depth = tc ? tc_pipeline_depth() : (fmt == 0 ? q4_pipeline_depth() : fp8_pipeline_depth());
   p.n_tiles = (int)ceil_div(N, TILE_N);
   p.nst = ceil_div(K, p.stage_k);
   auto fix = [&](int S) {
@@ -111,22 +117,28 @@ Plan make_plan(int fmt, int64_t N, int64_t K, int sm_count, int forced_splits) {
     p.S = (int)ceil_div(p.nst, spc);
   };
   if (forced_splits > 0) {
-    fix((int)(forced_splits < p.nst ? forced_splits : p.nst));
+    int S = forced_splits < MAX_SPLITS ? forced_splits : MAX_SPLITS;
+    fix((int)(S < p.nst ? S : p.nst));
     return p;
   }
   const int64_t max_ctas = 2ll * sm_count;
   double best = 1e30;
   int best_s = 1;
-  for (int S = 1; S <= 64 && S <= p.nst; ++S) {
+  for (int S = 1; S <= MAX_SPLITS && S <= p.nst; ++S) {
     const int64_t spc = ceil_div(p.nst, S);
     if (ceil_div(p.nst, spc) != S) continue;
     const int64_t ctas = (int64_t)p.n_tiles * S;
-    if (S > 1 && ctas > max_ctas) break;
+    if (S > 1) {
+      if (ctas > max_ctas) break;
+      const int clusters = tc ? tc_max_active_clusters(S)
+                              : (fmt == 0 ? q4_max_active_clusters(S) : fp8_max_active_clusters(S));
+      if (clusters > 0 && p.n_tiles > clusters) continue;
+    }
     const double bytes = (double)ctas * spc * p.stage_bytes;
     double rate = (double)ctas * PLAN_CTA_BPS;
     if (rate > PLAN_HBM_BPS) rate = PLAN_HBM_BPS;
     double t = bytes / rate;
-    if (S > 1) t += PLAN_FIXUP_S + (double)ctas * TILE_N * MAX_M * 4 * 2 / PLAN_L2_BPS;
+    if (S > 1) t += PLAN_CLUSTER_REDUCE_S;
     if (t < best * 0.999) {
       best = t;
       best_s = S;
@@ -144,8 +156,6 @@ void free_handle(qmm_handle* h) {
   cudaFree(h->wdev);
   cudaFree(h->act_scratch);
   cudaFree(h->out_scale);
-  cudaFree(h->partial);
-  cudaFree(h->counters);
   cudaFree(h->status);
   cudaFree(h->stage_act);
   cudaFree(h->stage_out);
@@ -163,6 +173,57 @@ int check_device(int* dev, int* sms) {
     return QMM_ERR_DEVICE;
   if (major != 10 || minor != 3) return QMM_ERR_DEVICE;
   return QMM_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver (looked up once through the runtime).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D view of M activation rows for the tcgen05 kernel: dim 0 = 8 consecutive
+// 16-bit values, dim 1 = rows (stride lda), dim 2 = 8-column groups (stride 16
+// bytes); a box of 8 x 16 x 32 lands as [group][row][8 values], the canonical
+// no-swizzle K-major layout, with rows >= M and columns >= K read as zeros.
+cudaError_t encode_act_map(CUtensorMap* map, const void* base, int64_t lda, int M, int64_t K, bool f16) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {8, (cuuint64_t)M, (cuuint64_t)((K + 7) / 8)};
+  cuuint64_t strides[2] = {(cuuint64_t)lda * 2, 16};
+  cuuint32_t box[3] = {8, 16, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The verify kernel of the handle's plan.  The tcgen05 kernel reads the
+// caller's bf16 rows through a tensor map, re-encoded when they change.
+cudaError_t launch_verify_kernel(qmm_handle* h, const VerifyParams& vp, const VerifyLaunch& vl,
+                                 const uint16_t* act, int64_t lda, int M) {
+  if (!h->plan.tc) return h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
+  if (h->map_ptr != act || h->map_lda != lda || h->map_M != M) {
+    cudaError_t e = encode_act_map(&h->act_map, act, lda, M, h->K, false);
+    if (e != cudaSuccess) {
+      h->map_ptr = nullptr;
+      return e;
+    }
+    h->map_ptr = act;
+    h->map_lda = lda;
+    h->map_M = M;
+  }
+  return launch_verify_tc(vp, &h->act_map, false, vl.ctas, vl.stream);
 }
 
 }  // namespace
@@ -195,7 +256,8 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   *out = nullptr;
   if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
   if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
-  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
+  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_MMA_SYNC))
+    return QMM_ERR_INVALID_ARG;
   if (d->k_splits < 0) return QMM_ERR_INVALID_ARG;
   const int fmt = (int)d->format;
   if (fmt == 1 && !d->scales) return QMM_ERR_INVALID_ARG;
@@ -216,18 +278,21 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   h->flags = d->flags;
   h->N = d->N;
   h->K = d->K;
-  h->plan = make_plan(fmt, d->N, d->K, sms, d->k_splits);
-  const Plan& p = h->plan;
-  const int64_t stages_total = (int64_t)p.S * p.spc;
-
-  cudaError_t e = fmt == 0 ? prepare_q4_attributes() : prepare_fp8_attributes();
+  // bf16 Q4_0 runs on the tcgen05 kernel; the f16 paths, the CUDA-core
+  // baseline and QMM_FLAG_MMA_SYNC use the mma.sync kernels.
+  const bool tc = fmt == 0 &&
+                  !(d->flags & (QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_MMA_SYNC));
+  cudaError_t e = tc ? prepare_tc_attributes()
+                     : (fmt == 0 ? prepare_q4_attributes() : prepare_fp8_attributes());
   if (e != cudaSuccess) {
     free_handle(h);
     return cuda_fail(nullptr, e);
   }
+  h->plan = make_plan(fmt, tc, d->N, d->K, sms, d->k_splits);
+  const Plan& p = h->plan;
+  const int64_t stages_total = (int64_t)p.S * p.spc;
   h->wdev_bytes = (size_t)p.n_tiles * stages_total * p.stage_bytes;
   h->act_bytes = (size_t)stages_total * act_stage_bytes(p.stage_k);
-  h->partial_bytes = (size_t)p.n_tiles * p.S * MAX_M * TILE_N * sizeof(float);
   h->stage_act_pitch = ceil_div(d->K, 8) * 8;
   void* tmp_w = nullptr;
   void* tmp_s = nullptr;
@@ -247,8 +312,6 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   QMM_ALLOC(h->wdev, h->wdev_bytes);
   QMM_ALLOC(h->act_scratch, h->act_bytes);
   QMM_ALLOC(h->out_scale, (size_t)MAX_M * p.S * sizeof(float));
-  QMM_ALLOC(h->partial, h->partial_bytes);
-  QMM_ALLOC(h->counters, (size_t)p.n_tiles * sizeof(int));
   QMM_ALLOC(h->status, sizeof(int));
   QMM_ALLOC(h->stage_act, (size_t)MAX_M * h->stage_act_pitch * sizeof(uint16_t));
   QMM_ALLOC(h->stage_out, (size_t)MAX_M * d->N * sizeof(float));
@@ -270,10 +333,10 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
     }
   }
 #undef QMM_ALLOC
-  if ((e = launch_repack(fmt, wsrc, ssrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st)) != cudaSuccess)
-    goto fail;
+  e = p.tc ? launch_repack_tc(wsrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st)
+           : launch_repack(fmt, wsrc, ssrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st);
+  if (e != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->act_scratch, 0, h->act_bytes, st)) != cudaSuccess) goto fail;
-  if ((e = cudaMemsetAsync(h->counters, 0, (size_t)p.n_tiles * sizeof(int), st)) != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) goto fail;
   cudaFree(tmp_w);
@@ -317,26 +380,32 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
   const bool f16 = had || h->fmt == 1;
 
-  PrepParams pp;
-  pp.act = act;
-  pp.lda = lda;
-  pp.out = h->act_scratch;
-  pp.out_scale = h->out_scale;
-  pp.K = h->K;
-  pp.M = M;
-  pp.S = p.S;
-  pp.spc = p.spc;
-  pp.stage_k = p.stage_k;
-  cudaError_t e = launch_act_prep(pp, f16, had, st);
-  if (e != cudaSuccess) return cuda_fail(h, e);
+  // bf16 operands read the caller's rows directly; the f16 paths (Hadamard
+  // rotation, FP8) go through the activation pre-pass and its scratch.
+  cudaError_t e = cudaSuccess;
+  if (f16) {
+    PrepParams pp;
+    pp.act = act;
+    pp.lda = lda;
+    pp.out = h->act_scratch;
+    pp.out_scale = h->out_scale;
+    pp.K = h->K;
+    pp.M = M;
+    pp.S = p.S;
+    pp.spc = p.spc;
+    pp.stage_k = p.stage_k;
+    e = launch_act_prep(pp, f16, had, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
 
   VerifyParams vp;
   vp.wdev = h->wdev;
-  vp.act = reinterpret_cast<const uint8_t*>(h->act_scratch);
-  vp.out_scale = h->out_scale;
+  vp.act = f16 ? reinterpret_cast<const uint8_t*>(h->act_scratch) : nullptr;
+  vp.act_rows = act;
+  vp.lda = lda;
+  vp.K = h->K;
+  vp.out_scale = f16 ? h->out_scale : nullptr;
   vp.out = out;
-  vp.partial = h->partial;
-  vp.counters = h->counters;
   vp.status = h->status;
   vp.ldo = ldo;
   vp.N = h->N;
@@ -350,7 +419,7 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
   vl.ctas = p.n_tiles * p.S;
   vl.stream = st;
-  e = h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
+  e = launch_verify_kernel(h, vp, vl, act, lda, M);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
 }
@@ -387,9 +456,8 @@ int qmm_sync_status(qmm_t h, void* stream) {
   e = cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (word != 0) {
-    // A kernel gave up: its split counters may be half-counted.  Reset.
+    // A kernel gave up: clear the word so the handle can be used again.
     cudaMemset(h->status, 0, sizeof(int));
-    cudaMemset(h->counters, 0, (size_t)h->plan.n_tiles * sizeof(int));
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(h, e);
     return QMM_ERR_TIMEOUT;
@@ -414,8 +482,7 @@ int qmm_get_info(qmm_t h, qmm_info* info) {
   info->weight_bytes = h->fmt == 0 ? h->N * h->K / 32 * 18
                                    : h->N * h->K + 4 * (h->N / 128) * (h->K / 128);
   info->device_weight_bytes = (int64_t)h->wdev_bytes;
-  info->scratch_bytes = (int64_t)(h->act_bytes + h->partial_bytes + MAX_M * p.S * sizeof(float) +
-                                  p.n_tiles * sizeof(int) + sizeof(int));
+  info->scratch_bytes = (int64_t)(h->act_bytes + MAX_M * p.S * sizeof(float) + sizeof(int));
   info->n_tiles = p.n_tiles;
   info->k_splits = p.S;
   info->ctas = p.n_tiles * p.S;
@@ -433,8 +500,10 @@ int qmm_dequantize(qmm_t h, float* w_out, void* stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
   const Plan& p = h->plan;
-  cudaError_t e = launch_dequant(h->fmt, h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
-                                 (cudaStream_t)stream);
+  cudaError_t e = p.tc ? launch_dequant_tc(h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
+                                           (cudaStream_t)stream)
+                       : launch_dequant(h->fmt, h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
+                                        (cudaStream_t)stream);
   return e == cudaSuccess ? QMM_OK : cuda_fail(h, e);
 }
 
@@ -531,44 +600,43 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
   const Plan& p = h->plan;
-  // Carve the array: activation scratch | row factors | split partials | split counters.
+  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
+  const bool f16 = had || h->fmt == 1;
+  // Carve the array: activation scratch | per-(row, split) factors.  Both are
+  // written in full by the pre-pass before the verify kernel reads them, so
+  // nothing has to be cleared; the bf16 path reads the caller's rows and uses
+  // no working memory at all.
   const size_t act_off = 0;
   const size_t scale_off = align256(act_off + h->act_bytes);
-  const size_t part_off = align256(scale_off + (size_t)MAX_M * p.S * sizeof(float));
-  const size_t cnt_off = align256(part_off + h->partial_bytes);
-  const size_t total = cnt_off + (size_t)p.n_tiles * sizeof(int);
-  if (total > STATIC_SCRATCH_BYTES) return QMM_ERR_SHAPE;
+  const size_t total = scale_off + (size_t)MAX_M * p.S * sizeof(float);
+  if (f16 && total > STATIC_SCRATCH_BYTES) return QMM_ERR_SHAPE;
   unsigned char* base = nullptr;
   cudaError_t e = static_scratch_addr(dev, &base);
   if (e != cudaSuccess) return cuda_fail(h, e);
   cudaStream_t st = (cudaStream_t)stream;
-  int* counters = reinterpret_cast<int*>(base + cnt_off);
-  // The split counters must start at zero; the array keeps the last call's contents.
-  e = cudaMemsetAsync(counters, 0, (size_t)p.n_tiles * sizeof(int), st);
-  if (e != cudaSuccess) return cuda_fail(h, e);
-
-  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
-  const bool f16 = had || h->fmt == 1;
-  PrepParams pp;
-  pp.act = act;
-  pp.lda = lda;
-  pp.out = reinterpret_cast<uint16_t*>(base + act_off);
-  pp.out_scale = reinterpret_cast<float*>(base + scale_off);
-  pp.K = h->K;
-  pp.M = M;
-  pp.S = p.S;
-  pp.spc = p.spc;
-  pp.stage_k = p.stage_k;
-  e = launch_act_prep(pp, f16, had, st);
-  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (f16) {
+    PrepParams pp;
+    pp.act = act;
+    pp.lda = lda;
+    pp.out = reinterpret_cast<uint16_t*>(base + act_off);
+    pp.out_scale = reinterpret_cast<float*>(base + scale_off);
+    pp.K = h->K;
+    pp.M = M;
+    pp.S = p.S;
+    pp.spc = p.spc;
+    pp.stage_k = p.stage_k;
+    e = launch_act_prep(pp, f16, had, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
 
   VerifyParams vp;
   vp.wdev = h->wdev;
-  vp.act = base + act_off;
-  vp.out_scale = reinterpret_cast<const float*>(base + scale_off);
+  vp.act = f16 ? base + act_off : nullptr;
+  vp.act_rows = act;
+  vp.lda = lda;
+  vp.K = h->K;
+  vp.out_scale = f16 ? reinterpret_cast<const float*>(base + scale_off) : nullptr;
   vp.out = out;
-  vp.partial = reinterpret_cast<float*>(base + part_off);
-  vp.counters = counters;
   vp.status = h->status;
   vp.ldo = ldo;
   vp.N = h->N;
@@ -582,7 +650,7 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
   vl.ctas = p.n_tiles * p.S;
   vl.stream = st;
-  e = h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
+  e = launch_verify_kernel(h, vp, vl, act, lda, M);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
 }

@@ -177,7 +177,7 @@ __global__ void repack_q4_kernel(const uint8_t* __restrict__ blocks, int64_t N, 
   const int lane = (int)(gt & 31);
   int64_t u = gt >> 5;
   const int r = (int)(u % 8); u /= 8;
-  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
   const int64_t stage_global = u;  // ((tile * S + split) * spc + i)
   const int i = (int)(u % spc); u /= spc;
   const int split = (int)(u % S);
@@ -220,7 +220,7 @@ __global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float
   const int lane = (int)(gt & 31);
   int64_t u = gt >> 5;
   const int r = (int)(u % 8); u /= 8;
-  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
   const int64_t stage_global = u;
   const int i = (int)(u % spc); u /= spc;
   const int split = (int)(u % S);
@@ -250,7 +250,7 @@ __global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float
     const int64_t tk_n = K / 128;
     float s = 0.f;
     if (tile * TILE_N < N && kt * 128 < K) s = scales[tile * tk_n + kt];
-    *reinterpret_cast<float4*>(stage + CONSUMER_WARPS * 8 * F8_UNIT_BYTES) = make_float4(s, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(stage + STAGE_CHUNKS * 8 * F8_UNIT_BYTES) = make_float4(s, 0.f, 0.f, 0.f);
   }
 }
 
@@ -265,7 +265,7 @@ __global__ void dequant_q4_kernel(const uint8_t* __restrict__ wdev, int64_t N, i
   const int lane = (int)(gt & 31);
   int64_t u = gt >> 5;
   const int r = (int)(u % 8); u /= 8;
-  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
   const int64_t stage_global = u;
   const int i = (int)(u % spc); u /= spc;
   const int split = (int)(u % S);
@@ -301,7 +301,7 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, int64_t N, 
   const int lane = (int)(gt & 31);
   int64_t u = gt >> 5;
   const int r = (int)(u % 8); u /= 8;
-  const int c = (int)(u % CONSUMER_WARPS); u /= CONSUMER_WARPS;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
   const int64_t stage_global = u;
   const int i = (int)(u % spc); u /= spc;
   const int split = (int)(u % S);
@@ -310,7 +310,7 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, int64_t N, 
   const int64_t kbase = ((int64_t)split * spc + i) * F8_STAGE_K + 32 * c;
   const uint8_t* stage = wdev + stage_global * F8_STAGE_BYTES;
   const uint8_t* unit = stage + (int64_t)(c * 8 + r) * F8_UNIT_BYTES;
-  const float s = *reinterpret_cast<const float*>(stage + CONSUMER_WARPS * 8 * F8_UNIT_BYTES);
+  const float s = *reinterpret_cast<const float*>(stage + STAGE_CHUNKS * 8 * F8_UNIT_BYTES);
   const uint4 cw = *reinterpret_cast<const uint4*>(unit + 16 * lane);
   const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -509,7 +509,7 @@ cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int 
 
 cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
                           int n_tiles, int S, int spc, uint8_t* wdev, cudaStream_t st) {
-  const int64_t units = (int64_t)n_tiles * S * spc * CONSUMER_WARPS * 8;
+  const int64_t units = (int64_t)n_tiles * S * spc * STAGE_CHUNKS * 8;
   const int64_t threads = units * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)
@@ -521,7 +521,7 @@ cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int
 
 cudaError_t launch_dequant(int fmt, const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S,
                            int spc, float* out, cudaStream_t st) {
-  const int64_t units = (int64_t)n_tiles * S * spc * CONSUMER_WARPS * 8;
+  const int64_t units = (int64_t)n_tiles * S * spc * STAGE_CHUNKS * 8;
   const int64_t threads = units * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)

@@ -41,18 +41,19 @@
 namespace qmm {
 
 constexpr int TILE_N = 128;           // rows of W per CTA tile
-constexpr int CONSUMER_WARPS = 4;     // warps that compute
-constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;  // + one producer warp
+constexpr int STAGE_CHUNKS = 4;       // column chunks per stage in the layout
+constexpr int COMPUTE_WARPS = 8;      // warps that compute: chunk x half of the tile's rows
+constexpr int THREADS = (COMPUTE_WARPS + 1) * 32;  // + one producer warp
 constexpr int MAX_M = 16;
 
 // Q4_0
 constexpr int Q4_STAGE_K = 256;
 constexpr int Q4_UNIT_BYTES = 576;
-constexpr int Q4_STAGE_BYTES = CONSUMER_WARPS * 8 * Q4_UNIT_BYTES;  // 18432
+constexpr int Q4_STAGE_BYTES = STAGE_CHUNKS * 8 * Q4_UNIT_BYTES;  // 18432
 // FP8
 constexpr int F8_STAGE_K = 128;
 constexpr int F8_UNIT_BYTES = 512;
-constexpr int F8_STAGE_BYTES = CONSUMER_WARPS * 8 * F8_UNIT_BYTES + 16;  // 16400
+constexpr int F8_STAGE_BYTES = STAGE_CHUNKS * 8 * F8_UNIT_BYTES + 16;  // 16400
 
 __host__ __device__ constexpr int act_pitch(int stage_k) { return stage_k + 8; }
 __host__ __device__ constexpr int act_stage_bytes(int stage_k) {
@@ -66,16 +67,17 @@ constexpr int DEV_ERR_TIMEOUT_DRAIN = 4;  // copies in flight did not land in ti
 
 struct VerifyParams {
   const uint8_t* wdev;       // repacked weights
-  const uint8_t* act;        // activation scratch (16-bit values, stage order)
-  const float* out_scale;    // [MAX_M][S]: multiplier of split s's partial for row m
+  const uint8_t* act;        // activation scratch (16-bit values, stage order), or NULL
+  const uint16_t* act_rows;  // the caller's bf16 rows (used when act is NULL)
+  int64_t lda;               // row stride of act_rows
+  int64_t K;                 // true K (bytes past it are not copied from act_rows)
+  const float* out_scale;    // [MAX_M][S]: multiplier of split s's partial for row m, or NULL
   float* out;                // [M][ldo]
-  float* partial;            // [n_tiles][S][MAX_M][TILE_N]
-  int* counters;             // [n_tiles], zero between launches
   int* status;               // device error word
   int64_t ldo;
   int64_t N;
   int M;
-  int S;                     // K splits
+  int S;                     // K splits = CTAs per cluster
   int spc;                   // stages per CTA
   uint64_t wait_limit_ns;    // bounded waits give up after this (0: at once)
 };
@@ -141,16 +143,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait for the phase of parity `parity` of barrier `bar`; give up after
+// Wait for the phase of parity `parity` of barrier `bar`; give up after about
 // `limit_ns` nanoseconds (limit 0: give up at once).  Returns true on success.
+// The deadline is kept in SM clock cycles (clock64 is cheap to read, unlike the
+// global timer) at 2 cycles per nanosecond, so at clocks below 2 GHz the wait
+// lasts proportionally longer before it gives up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
   if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
+  const long long limit = (long long)(limit_ns < (1ull << 40) ? limit_ns : (1ull << 40)) * 2;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 
@@ -178,6 +184,31 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Thread-block clusters: barrier over every thread of every CTA of the
+// cluster (release/acquire), and loads from another CTA's shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 
 // Programmatic dependent launch.

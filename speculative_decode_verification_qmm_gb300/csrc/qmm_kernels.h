@@ -25,6 +25,23 @@ size_t q4_smem_bytes();
 size_t fp8_smem_bytes();
 cudaError_t prepare_q4_attributes();
 cudaError_t prepare_fp8_attributes();
+// Clusters of S CTAs the device can hold at once (-1 if the query fails).
+int q4_max_active_clusters(int S);
+int fp8_max_active_clusters(int S);
+constexpr int MAX_SPLITS = 16;  // K splits = cluster size (16 needs the non-portable opt-in)
+
+// tcgen05 kernel (Q4_0): its weight layout, repack, dequantization and launch.
+// act_map points to a CUtensorMap over the activation rows (3-D view
+// [K/8 groups][M rows][8 values], boxes of 32 x 16 x 8).
+cudaError_t prepare_tc_attributes();
+int tc_max_active_clusters(int S);
+int tc_pipeline_depth();
+cudaError_t launch_verify_tc(const VerifyParams& vp, const void* act_map, bool f16_ops, int ctas,
+                             cudaStream_t st);
+cudaError_t launch_repack_tc(const uint8_t* blocks, int64_t N, int64_t K, int n_tiles, int S, int spc,
+                             uint8_t* wdev, cudaStream_t st);
+cudaError_t launch_dequant_tc(const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S, int spc,
+                              float* out, cudaStream_t st);
 
 cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l);
 cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l);

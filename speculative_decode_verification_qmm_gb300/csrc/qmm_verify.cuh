@@ -1,18 +1,22 @@
 // qmm_verify.cuh -- the weight-streaming verify kernel.
 //
 // One CTA = one row tile of W (128 rows) x one K split.  A producer warp
-// streams the CTA's stages (weights: one bulk copy; activations of the drafted
-// rows: one bulk copy) through an NS-deep shared-memory ring guarded by
-// mbarriers.  Four consumer warps each own one quarter of every stage's K
-// range for all 128 rows: they dequantize codes in registers straight into
-// mma.sync A fragments (weights are the MMA's M dimension, the drafted rows
-// its N = 8 or 16 dimension, "swap AB"), keep fp32 accumulators in registers
-// across the whole K range, and apply the per-block (Q4_0) or per-tile (FP8)
-// scale with packed fp32 FMAs.  The epilogue sums the four warps in a fixed
-// order through shared memory, multiplies by the activation pre-pass's
-// per-(row, split) power-of-two factor and either writes `out` (one split) or
-// writes a partial and lets the last-arriving split of the tile add all
-// partials in split order (deterministic, no spinning).
+// streams the CTA's stages through an NS-deep shared-memory ring guarded by
+// mbarriers: per stage one bulk copy of the repacked weights and one bulk copy
+// per drafted row of the activations (straight from the caller's bf16 rows, or
+// from the pre-pass scratch on the f16 paths).  Eight compute warps split every
+// stage into four column chunks x two halves of the tile's rows; each warp
+// dequantizes its codes in registers straight into mma.sync A fragments
+// (weights are the MMA's M dimension, drafted rows its N = 8 or 16 dimension,
+// "swap AB"), keeps fp32 accumulators in registers across the CTA's K range,
+// and applies the per-block (Q4_0) or per-tile (FP8) scale with packed fp32
+// FMAs.  The epilogue adds the four chunk partials in a fixed order through
+// shared memory, multiplies by the pre-pass's per-(row, split) power-of-two
+// factor, and either writes `out` (one split) or, when the K range is split,
+// leaves its partial in shared memory: the S CTAs of a row tile form one
+// thread-block cluster and each adds a slice of the tile's rows over the S
+// partials through distributed shared memory, in split order (deterministic,
+// no global scratch, no atomics).
 //
 // The summation order of every output element is fixed by (N, K, plan) and
 // never depends on M, so row m of the result is bit-identical for M = 1..16.
@@ -32,7 +36,7 @@ struct FmtTraits<0> {  // Q4_0
   static constexpr int STAGE_K = Q4_STAGE_K;
   static constexpr int STAGE_BYTES = Q4_STAGE_BYTES;
   static constexpr int UNIT_BYTES = Q4_UNIT_BYTES;
-  static constexpr int CHUNK_K = STAGE_K / CONSUMER_WARPS;  // 64
+  static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 64
 };
 
 template <>
@@ -40,21 +44,32 @@ struct FmtTraits<1> {  // FP8 E4M3, 128x128 scales
   static constexpr int STAGE_K = F8_STAGE_K;
   static constexpr int STAGE_BYTES = F8_STAGE_BYTES;
   static constexpr int UNIT_BYTES = F8_UNIT_BYTES;
-  static constexpr int CHUNK_K = STAGE_K / CONSUMER_WARPS;  // 32
+  static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 32
 };
+
+// Row subtiles (16 rows) per compute warp: the 8 subtiles of a tile are split
+// into two halves.
+constexpr int WARP_SUBTILES = 8 * STAGE_CHUNKS / COMPUTE_WARPS;  // 4
+static_assert(WARP_SUBTILES * 2 == 8, "two row halves per chunk");
 
 template <int FMT, int NS>
 struct SmemLayout {
   using F = FmtTraits<FMT>;
   static constexpr int W_OFF = 0;
   static constexpr int A_OFF = NS * F::STAGE_BYTES;
-  static constexpr int BAR_OFF = A_OFF + NS * act_stage_bytes(F::STAGE_K);
+  static constexpr int A_BYTES = NS * act_stage_bytes(F::STAGE_K);
+  static constexpr int BAR_OFF = A_OFF + A_BYTES;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NS * 8;
   static constexpr int BYTES = FLAG_OFF + 16;
-  // epilogue reduction area (reuses the weight ring)
+  // epilogue areas (reuse the weight ring): chunk partials [chunk][row][RED_PITCH],
+  // then the CTA partial read by the cluster [row][CP_PITCH]
   static constexpr int RED_PITCH = MAX_M + 2;  // floats per row
-  static constexpr int RED_BYTES = CONSUMER_WARPS * TILE_N * RED_PITCH * 4;
-  static_assert(RED_BYTES <= NS * F::STAGE_BYTES, "reduction area must fit in the ring");
+  static constexpr int RED_BYTES = STAGE_CHUNKS * TILE_N * RED_PITCH * 4;
+  static constexpr int CP_PITCH = MAX_M + 1;
+  static constexpr int CP_OFF = RED_BYTES;
+  static constexpr int CP_BYTES = TILE_N * CP_PITCH * 4;
+  static_assert(CP_OFF + CP_BYTES <= NS * F::STAGE_BYTES, "epilogue areas must fit in the ring");
+  static_assert(A_OFF % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
 };
 
 // e4m3 pair (16 bits) -> f16x2, exact.
@@ -66,28 +81,32 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
   return r;
 }
 
+// B fragments for NSTEP k16 steps of the activation chunk at `abase`:
+// b[s][0..1] serve draft rows 0..7, b[s][2..3] rows 8..15.
+template <int NSTEP, int STAGE_K>
+__device__ __forceinline__ void load_b_frags(uint32_t abase, int lane, uint32_t (&b)[NSTEP][4]) {
+  const int row = (lane & 7) + ((lane >> 4) << 3);
+  const int koff = ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int s = 0; s < NSTEP; ++s) {
+    const uint32_t addr = abase + (uint32_t)(row * act_pitch(STAGE_K) + s * 16 + koff) * 2u;
+    ldmatrix_x4(addr, b[s][0], b[s][1], b[s][2], b[s][3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
-// Consumer compute for one stage.  acc[r][j][0..3] is the C fragment of row
-// subtile r (16 rows) and draft-row tile j (8 columns).
+// Compute for one stage and one warp.  acc[r][j][0..3] is the C fragment of
+// the warp's row subtile r (16 rows) and draft-row tile j (8 columns).
 // ---------------------------------------------------------------------------
 template <typename Op, int NT8>
 __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, int lane,
-                                             float (&acc)[8][2][4]) {
+                                             float (&acc)[WARP_SUBTILES][2][4]) {
   const int g = lane >> 2;
-  // B fragments for the warp's 64 columns: 4 k16 steps x (b0, b1) x NT8 tiles.
   uint32_t b[4][4];
-  {
-    const int row = (lane & 7) + ((lane >> 4) << 3);
-    const int koff = ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint32_t addr = abase + (uint32_t)(row * act_pitch(Q4_STAGE_K) + s * 16 + koff) * 2u;
-      ldmatrix_x4(addr, b[s][0], b[s][1], b[s][2], b[s][3]);
-    }
-  }
+  load_b_frags<4, Q4_STAGE_K>(abase, lane, b);
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
+  for (int r = 0; r < WARP_SUBTILES; ++r) {
     const uint32_t unit = wunit0 + (uint32_t)(r * Q4_UNIT_BYTES);
     const uint4 codes = lds128(unit + 16u * lane);
     const uint2 sc = lds64(unit + 512u + 8u * g);
@@ -102,11 +121,11 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
       const float dg8 = __half2float(__ushort_as_half((unsigned short)(dpair >> 16)));
 #pragma unroll
       for (int j = 0; j < NT8; ++j) {
-        float p[4];
-        Op::mma(p, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], zero);
-        Op::mma(p, a1[0], a1[1], a1[2], a1[3], b[2 * blk + 1][2 * j], b[2 * blk + 1][2 * j + 1], p);
-        ffma2(acc[r][j][0], acc[r][j][1], dg, p[0], p[1]);
-        ffma2(acc[r][j][2], acc[r][j][3], dg8, p[2], p[3]);
+        float pp[4];
+        Op::mma(pp, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], zero);
+        Op::mma(pp, a1[0], a1[1], a1[2], a1[3], b[2 * blk + 1][2 * j], b[2 * blk + 1][2 * j + 1], pp);
+        ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
+        ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);
       }
     }
   }
@@ -114,93 +133,81 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
 
 template <int NT8>
 __device__ __forceinline__ void f8_stage_mma(uint32_t wunit0, uint32_t abase, float s, int lane,
-                                             float (&acc)[8][2][4]) {
+                                             float (&acc)[WARP_SUBTILES][2][4]) {
   uint32_t b[2][4];
-  {
-    const int row = (lane & 7) + ((lane >> 4) << 3);
-    const int koff = ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int st = 0; st < 2; ++st) {
-      const uint32_t addr = abase + (uint32_t)(row * act_pitch(F8_STAGE_K) + st * 16 + koff) * 2u;
-      ldmatrix_x4(addr, b[st][0], b[st][1], b[st][2], b[st][3]);
-    }
-  }
+  load_b_frags<2, F8_STAGE_K>(abase, lane, b);
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
+  for (int r = 0; r < WARP_SUBTILES; ++r) {
     const uint4 codes = lds128(wunit0 + (uint32_t)(r * F8_UNIT_BYTES) + 16u * lane);
-    // word v: step j = v / 2, half h = v % 2 -> A registers (a0, a1) or (a2, a3)
+    // word v: k16 step v / 2, half v % 2 -> A registers (a0, a1) or (a2, a3)
     const uint32_t a00 = e4m3x2_to_f16x2(codes.x & 0xFFFFu), a01 = e4m3x2_to_f16x2(codes.x >> 16);
     const uint32_t a02 = e4m3x2_to_f16x2(codes.y & 0xFFFFu), a03 = e4m3x2_to_f16x2(codes.y >> 16);
     const uint32_t a10 = e4m3x2_to_f16x2(codes.z & 0xFFFFu), a11 = e4m3x2_to_f16x2(codes.z >> 16);
     const uint32_t a12 = e4m3x2_to_f16x2(codes.w & 0xFFFFu), a13 = e4m3x2_to_f16x2(codes.w >> 16);
 #pragma unroll
     for (int j = 0; j < NT8; ++j) {
-      float p[4];
-      F16Op::mma(p, a00, a01, a02, a03, b[0][2 * j], b[0][2 * j + 1], zero);
-      F16Op::mma(p, a10, a11, a12, a13, b[1][2 * j], b[1][2 * j + 1], p);
-      ffma2(acc[r][j][0], acc[r][j][1], s, p[0], p[1]);
-      ffma2(acc[r][j][2], acc[r][j][3], s, p[2], p[3]);
+      float pp[4];
+      F16Op::mma(pp, a00, a01, a02, a03, b[0][2 * j], b[0][2 * j + 1], zero);
+      F16Op::mma(pp, a10, a11, a12, a13, b[1][2 * j], b[1][2 * j + 1], pp);
+      ffma2(acc[r][j][0], acc[r][j][1], s, pp[0], pp[1]);
+      ffma2(acc[r][j][2], acc[r][j][3], s, pp[2], pp[3]);
     }
   }
 }
 
-// CUDA-core baseline for Q4_0: fp32 dequantization and one FFMA per weight and
+// CUDA-core baseline for Q4_0: fp32 dequantization and one FMA per weight and
 // drafted row; each lane accumulates its own columns and the four lanes of a
 // group are added with warp shuffles at the end (split K inside the warp).
-// Here warps own row subtiles {2w, 2w+1} over all four chunks of the stage.
+// Warp w owns row subtile w over all four chunks of every stage.
 template <typename T, int NT8>
-__device__ __forceinline__ void q4_stage_simt(uint32_t wstage, uint32_t abase, int warp, int lane,
-                                              int M, float (&acc)[2][2][MAX_M]) {
+__device__ __forceinline__ void q4_stage_simt(uint32_t wstage, uint32_t astage, int warp, int lane,
+                                              int M, float (&acc)[2][MAX_M]) {
   const int g = lane >> 2, t = lane & 3;
   constexpr int MR = 8 * NT8;
 #pragma unroll 1
-  for (int c = 0; c < CONSUMER_WARPS; ++c) {
+  for (int c = 0; c < STAGE_CHUNKS; ++c) {
+    const uint32_t unit = wstage + (uint32_t)((c * 8 + warp) * Q4_UNIT_BYTES);
+    const uint4 codes = lds128(unit + 16u * lane);
+    const uint2 sc = lds64(unit + 512u + 8u * g);
+    const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int r = 2 * warp + rr;
-      const uint32_t unit = wstage + (uint32_t)((c * 8 + r) * Q4_UNIT_BYTES);
-      const uint4 codes = lds128(unit + 16u * lane);
-      const uint2 sc = lds64(unit + 512u + 8u * g);
-      const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint32_t dpair = blk ? sc.y : sc.x;
+      const float d[2] = {__half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF))),
+                          __half2float(__ushort_as_half((unsigned short)(dpair >> 16)))};
+      float part[2][MR];
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        const uint32_t dpair = blk ? sc.y : sc.x;
-        const float d[2] = {__half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF))),
-                            __half2float(__ushort_as_half((unsigned short)(dpair >> 16)))};
-        float part[2][MR];
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int m = 0; m < MR; ++m) part[h][m] = 0.f;
 #pragma unroll
-          for (int m = 0; m < MR; ++m) part[h][m] = 0.f;
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t w = words[2 * blk + j];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t w = words[2 * blk + j];
+        for (int pn = 0; pn < 8; ++pn) {
+          const int pair = pn & 3, half = pn >> 2;
+          const int h = pair & 1;  // row g or g + 8
+          const int k = c * 64 + 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);
+          const float qv = __int_as_float(0x4B000000 | ((w >> (4 * pn)) & 15u)) - 8388616.0f;
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const int pair = p & 3, half = p >> 2;
-            const int h = pair & 1;  // row g or g + 8
-            const int k = c * 64 + 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);
-            const float q = __int_as_float(0x4B000000 | ((w >> (4 * p)) & 15u)) - 8388616.0f;
-#pragma unroll
-            for (int m = 0; m < MR; ++m) {
-              if (m < M) {
-                const uint32_t bits = lds_u16(abase + (uint32_t)(m * act_pitch(Q4_STAGE_K) + k) * 2u);
-                float a;
-                if constexpr (std::is_same<T, __nv_bfloat16>::value)
-                  a = __uint_as_float(bits << 16);
-                else
-                  a = __half2float(__ushort_as_half((unsigned short)bits));
-                part[h][m] = fmaf(q, a, part[h][m]);
-              }
+          for (int m = 0; m < MR; ++m) {
+            if (m < M) {
+              const uint32_t bits = lds_u16(astage + (uint32_t)(m * act_pitch(Q4_STAGE_K) + k) * 2u);
+              float a;
+              if constexpr (std::is_same<T, __nv_bfloat16>::value)
+                a = __uint_as_float(bits << 16);
+              else
+                a = __half2float(__ushort_as_half((unsigned short)bits));
+              part[h][m] = fmaf(qv, a, part[h][m]);
             }
           }
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int m = 0; m < MR; ++m) acc[rr][h][m] = fmaf(d[h], part[h][m], acc[rr][h][m]);
       }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[h][m] = fmaf(d[h], part[h][m], acc[h][m]);
     }
   }
 }
@@ -217,6 +224,7 @@ template <int FMT, typename Op, int NT8, bool SIMT, int NS>
 __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constant__ VerifyParams p) {
   using F = FmtTraits<FMT>;
   using L = SmemLayout<FMT, NS>;
+  constexpr int PITCH_B = act_pitch(F::STAGE_K) * 2;  // bytes per activation row in shared memory
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -232,20 +240,14 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
   // [0] abort, [1] this CTA adds the split partials, [2] stages issued by the producer
   volatile int* s_flag = reinterpret_cast<volatile int*>(smem + L::FLAG_OFF);
 
-  // Rows >= M of every activation slot are never written by the copies: zero them.
-  {
-    constexpr int ROW_BYTES = act_pitch(F::STAGE_K) * 2;
-    const int zbytes = (MAX_M - M) * ROW_BYTES;
-    for (int slot = 0; slot < NS; ++slot) {
-      uint8_t* base = smem + L::A_OFF + slot * act_stage_bytes(F::STAGE_K) + M * ROW_BYTES;
-      for (int i = tid * 16; i < zbytes; i += THREADS * 16)
-        *reinterpret_cast<uint4*>(base + i) = make_uint4(0, 0, 0, 0);
-    }
-  }
+  // Zero the activation ring: rows >= M are never copied, and in the last
+  // stage the columns past K must hold finite values (their weights are 0).
+  for (int i = tid * 16; i < L::A_BYTES; i += THREADS * 16)
+    *reinterpret_cast<uint4*>(smem + L::A_OFF + i) = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_empty + 8 * i, CONSUMER_WARPS);
+      mbar_init(s_empty + 8 * i, COMPUTE_WARPS);
     }
     s_flag[0] = 0;
     s_flag[1] = 0;
@@ -258,69 +260,94 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
   pdl_trigger();
 
   const int nst = p.spc;
-  const uint8_t* wsrc = p.wdev + (size_t)(tile * p.S + split) * nst * F::STAGE_BYTES;
-  const uint8_t* asrc = p.act + (size_t)split * nst * act_stage_bytes(F::STAGE_K);
-  const uint32_t abytes = (uint32_t)(M * act_pitch(F::STAGE_K) * 2);
+  const int64_t gstage0 = (int64_t)split * nst;  // global index of this CTA's first stage
+  const uint8_t* wsrc = p.wdev + ((size_t)tile * p.S + split) * nst * F::STAGE_BYTES;
+  const bool direct = (p.act == nullptr);
+  // activation bytes per drafted row for stage i, and the source of row m
+  auto row_bytes = [&](int i) -> uint32_t {
+    if (!direct) return (uint32_t)(F::STAGE_K * 2);
+    const int64_t k0 = (gstage0 + i) * F::STAGE_K;
+    int64_t v = p.K - k0;
+    v = v < 0 ? 0 : (v > F::STAGE_K ? F::STAGE_K : v);
+    return (uint32_t)(v * 2);
+  };
+  auto row_src = [&](int i, int m) -> const void* {
+    if (direct) return p.act_rows + (int64_t)m * p.lda + (gstage0 + i) * F::STAGE_K;
+    return p.act + (size_t)(gstage0 + i) * act_stage_bytes(F::STAGE_K) + (size_t)m * PITCH_B;
+  };
 
-  if (warp == CONSUMER_WARPS) {
+  if (warp == COMPUTE_WARPS) {
     // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    const int pre = nst < NS ? nst : NS;
+    // Weights never depend on earlier kernels: fetch the first stages now.
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const int pre = nst < NS ? nst : NS;
-      // Weights never depend on earlier kernels: fetch the first stages now.
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(s_full + 8 * i, F::STAGE_BYTES);
         bulk_g2s_hint(s_w + i * F::STAGE_BYTES, wsrc + (size_t)i * F::STAGE_BYTES, F::STAGE_BYTES,
                       s_full + 8 * i, pol);
       }
-      // Activations come from the pre-pass: wait for it.
-      pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(s_full + 8 * i, abytes);
-        bulk_g2s(s_a + i * act_stage_bytes(F::STAGE_K),
-                 asrc + (size_t)i * act_stage_bytes(F::STAGE_K), abytes, s_full + 8 * i);
-      }
-      int issued = pre;
-      for (int i = NS; i < nst; ++i) {
-        const int slot = i % NS;
-        if (!mbar_wait_bounded(s_empty + 8 * slot, ((i / NS) - 1) & 1, p.wait_limit_ns)) {
+    }
+    // Activations may be written by the previous kernel: wait for it.
+    pdl_wait();
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t rb = row_bytes(i);
+      if (lane == 0) mbar_arrive_expect_tx(s_full + 8 * i, rb * (uint32_t)M);
+      __syncwarp();
+      if (lane < M && rb)
+        bulk_g2s(s_a + i * act_stage_bytes(F::STAGE_K) + lane * PITCH_B, row_src(i, lane), rb,
+                 s_full + 8 * i);
+    }
+    int issued = pre;
+    for (int i = NS; i < nst; ++i) {
+      const int slot = i % NS;
+      int ok = 0;
+      if (lane == 0) {
+        ok = mbar_wait_bounded(s_empty + 8 * slot, ((i / NS) - 1) & 1, p.wait_limit_ns) ? 1 : 0;
+        if (!ok) {
           atomicOr(p.status, DEV_ERR_TIMEOUT_EMPTY);
           s_flag[0] = 1;
-          break;
         }
-        if (s_flag[0]) break;
-        issued = i + 1;
-        mbar_arrive_expect_tx(s_full + 8 * slot, F::STAGE_BYTES + abytes);
+        ok = ok && !s_flag[0];
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      const uint32_t rb = row_bytes(i);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(s_full + 8 * slot, F::STAGE_BYTES + rb * (uint32_t)M);
         bulk_g2s_hint(s_w + slot * F::STAGE_BYTES, wsrc + (size_t)i * F::STAGE_BYTES,
                       F::STAGE_BYTES, s_full + 8 * slot, pol);
-        bulk_g2s(s_a + slot * act_stage_bytes(F::STAGE_K),
-                 asrc + (size_t)i * act_stage_bytes(F::STAGE_K), abytes, s_full + 8 * slot);
       }
-      s_flag[2] = issued;
+      __syncwarp();
+      if (lane < M && rb)
+        bulk_g2s(s_a + slot * act_stage_bytes(F::STAGE_K) + lane * PITCH_B, row_src(i, lane), rb,
+                 s_full + 8 * slot);
+      issued = i + 1;
     }
+    if (lane == 0) s_flag[2] = issued;
   }
 
-  // Accumulators (registers) of the consumer warps.
-  float acc[8][2][4];
-  float accs[2][2][MAX_M];
+  // Accumulators (registers) of the compute warps.
+  float acc[WARP_SUBTILES][2][4];
+  float accs[2][MAX_M];
   if constexpr (!SIMT) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < WARP_SUBTILES; ++r)
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[r][j][e] = 0.f;
   } else {
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int m = 0; m < MAX_M; ++m) accs[a][b][m] = 0.f;
+      for (int m = 0; m < MAX_M; ++m) accs[h][m] = 0.f;
   }
 
-  if (warp < CONSUMER_WARPS) {
-    // ------------------------------------------------------------ consumers
+  const int chunk = warp & (STAGE_CHUNKS - 1);
+  const int sub0 = (warp / STAGE_CHUNKS) * WARP_SUBTILES;  // first row subtile of this warp
+  if (warp < COMPUTE_WARPS) {
+    // ------------------------------------------------------------ compute
     for (int i = 0; i < nst; ++i) {
       const int slot = i % NS;
       if (!mbar_wait_bounded(s_full + 8 * slot, (i / NS) & 1, p.wait_limit_ns)) {
@@ -336,12 +363,13 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
                                                   __half>::type,
                         NT8>(wst, ast, warp, lane, M, accs);
         } else {
-          q4_stage_mma<Op, NT8>(wst + warp * 8 * Q4_UNIT_BYTES, ast + warp * F::CHUNK_K * 2, lane,
-                                acc);
+          q4_stage_mma<Op, NT8>(wst + (chunk * 8 + sub0) * Q4_UNIT_BYTES,
+                                ast + chunk * F::CHUNK_K * 2, lane, acc);
         }
       } else {
         const float s = lds_f32(wst + (F::STAGE_BYTES - 16));
-        f8_stage_mma<NT8>(wst + warp * 8 * F8_UNIT_BYTES, ast + warp * F::CHUNK_K * 2, s, lane, acc);
+        f8_stage_mma<NT8>(wst + (chunk * 8 + sub0) * F8_UNIT_BYTES, ast + chunk * F::CHUNK_K * 2,
+                          s, lane, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + 8 * slot);
@@ -349,12 +377,13 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
     }
   }
   __syncthreads();
-  if (s_flag[0]) {
+  const bool aborted = s_flag[0] != 0;
+  if (aborted) {
     // Give up: no copy issued by this CTA may still be landing in shared memory
     // when the CTA exits.  Only the last NS issued stages can be in flight, and
     // each of them is the latest phase armed on its slot; its phase completes
-    // when its bytes land, whether or not a consumer waited for it.
-    if (warp == CONSUMER_WARPS && lane == 0) {
+    // when its bytes land, whether or not a compute warp waited for it.
+    if (warp == COMPUTE_WARPS && lane == 0) {
       const int issued = s_flag[2];
       for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i) {
         if (!mbar_wait_bounded(s_full + 8 * (i % NS), (i / NS) & 1, 1000000000ull))
@@ -362,92 +391,95 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
       }
     }
     __syncthreads();
-    return;
+    // An aborted CTA writes nothing but still takes part in the cluster
+    // barriers below, so that no CTA of its cluster can wait for it forever.
   }
 
   // ------------------------------------------------------------ epilogue
   pdl_wait();  // order our writes after every earlier kernel's
   float* red = reinterpret_cast<float*>(smem + L::W_OFF);
+  float* cpart = reinterpret_cast<float*>(smem + L::W_OFF + L::CP_OFF);
   constexpr int RP = L::RED_PITCH;
-  if (warp < CONSUMER_WARPS) {
+  constexpr int CP = L::CP_PITCH;
+  if (warp < COMPUTE_WARPS && !aborted) {
     const int g = lane >> 2, t = lane & 3;
     if constexpr (!SIMT) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < WARP_SUBTILES; ++r)
 #pragma unroll
         for (int j = 0; j < NT8; ++j) {
-          const int row = 16 * r + g, col = 8 * j + 2 * t;
-          float* d0 = red + (warp * TILE_N + row) * RP + col;
-          float* d1 = red + (warp * TILE_N + row + 8) * RP + col;
+          const int row = 16 * (sub0 + r) + g, col = 8 * j + 2 * t;
+          float* d0 = red + (chunk * TILE_N + row) * RP + col;
+          float* d1 = red + (chunk * TILE_N + row + 8) * RP + col;
           *reinterpret_cast<float2*>(d0) = make_float2(acc[r][j][0], acc[r][j][1]);
           *reinterpret_cast<float2*>(d1) = make_float2(acc[r][j][2], acc[r][j][3]);
         }
     } else {
       // add the four lanes of each group (their column subsets of K)
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int m = 0; m < MAX_M; ++m) {
-            float v = accs[rr][h][m];
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-            accs[rr][h][m] = v;
-          }
-      // the SIMT warps own distinct rows: reduction slot 0 holds every row
+        for (int m = 0; m < MAX_M; ++m) {
+          float v = accs[h][m];
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+          accs[h][m] = v;
+        }
       if (t == 0) {
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
+        for (int h = 0; h < 2; ++h) {
+          const int row = 16 * warp + g + 8 * h;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = 16 * (2 * warp + rr) + g + 8 * h;
-#pragma unroll
-            for (int m = 0; m < MAX_M; ++m) red[row * RP + m] = accs[rr][h][m];
-          }
+          for (int m = 0; m < MAX_M; ++m) red[row * RP + m] = accs[h][m];
+        }
       }
     }
   }
   __syncthreads();
 
-  const int64_t n = (int64_t)tile * TILE_N + tid;
-  if (tid < TILE_N) {
+  // The CTA's partial: the chunk partials added in chunk order, times the
+  // pre-pass's factor of this (row, split).
+  if (tid < TILE_N && !aborted) {
+    constexpr int NRED = SIMT ? 1 : STAGE_CHUNKS;
+    const int64_t n = (int64_t)tile * TILE_N + tid;
     for (int m = 0; m < M; ++m) {
-      constexpr int NRED = SIMT ? 1 : CONSUMER_WARPS;
       float v = red[tid * RP + m];
 #pragma unroll
-      for (int w = 1; w < NRED; ++w) v += red[(w * TILE_N + tid) * RP + m];
-      v *= p.out_scale[m * p.S + split];
+      for (int c = 1; c < NRED; ++c) v += red[(c * TILE_N + tid) * RP + m];
+      if (p.out_scale) v *= p.out_scale[m * p.S + split];
       if (p.S == 1) {
         if (n < p.N) p.out[(int64_t)m * p.ldo + n] = v;
       } else {
-        p.partial[(((size_t)tile * p.S + split) * MAX_M + m) * TILE_N + tid] = v;
+        cpart[tid * CP + m] = v;
       }
     }
   }
   if (p.S == 1) return;
 
-  // Split-K: the last split of this tile to arrive adds all partials in split order.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&p.counters[tile], 1);
-    s_flag[1] = (prev == p.S - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_flag[1]) return;
-  __threadfence();
-  if (tid < TILE_N) {
-    for (int m = 0; m < M; ++m) {
-      float v = 0.f;
-      for (int s = 0; s < p.S; ++s) {
-        const float x = __ldcg(&p.partial[(((size_t)tile * p.S + s) * MAX_M + m) * TILE_N + tid]);
-        v = (s == 0) ? x : v + x;
-      }
+  // Split K: the S CTAs of this row tile are one cluster.  CTA `split` adds
+  // the S partials of its slice of the tile's rows, in split order.
+  cluster_sync_all();
+  if (!aborted) {
+    const int r0 = (split * TILE_N) / p.S, r1 = ((split + 1) * TILE_N) / p.S;
+    const int nr = r1 - r0;
+    const uint32_t cbase = smem_u32(cpart);
+    for (int idx = tid; idx < nr * M; idx += THREADS) {
+      const int m = idx / nr, row = r0 + idx % nr;
+      const uint32_t la = cbase + (uint32_t)(row * CP + m) * 4u;
+      float x[16];
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < p.S) x[s] = ld_dsmem_f32(dsmem_map(la, (uint32_t)s));
+      float v = x[0];
+#pragma unroll
+      for (int s = 1; s < 16; ++s)
+        if (s < p.S) v += x[s];
+      const int64_t n = (int64_t)tile * TILE_N + row;
       if (n < p.N) p.out[(int64_t)m * p.ldo + n] = v;
     }
   }
-  if (tid == 0) p.counters[tile] = 0;
+  // Keep this CTA's shared memory alive until every CTA of the cluster has read it.
+  cluster_sync_all();
 }
 
 }  // namespace qmm

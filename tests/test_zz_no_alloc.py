@@ -67,10 +67,10 @@ def test_noalloc_matches_verify_on_consecutive_calls(fmt, N, K, M, hadamard, spl
 
 
 def test_noalloc_rejects_plans_beyond_the_array():
-    # one K split per 256-column stage on a wide matrix: partials need > 4 MiB
-    N, K = 8192, 8192
-    blocks = q.quantize_q4_0(synth.weights_cuda(N, K, 950))
-    mat = q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, k_splits=32)
+    # the rotated activations of K = 131328 columns need more than the 4 MiB array
+    N, K = 128, 131328
+    blocks = q.quantize_q4_0(synth.weights_cuda(N, K, 950), hadamard=True)
+    mat = q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=True)
     act = bf16_cuda(synth.activations(4, K, 951))
     out = torch.empty((4, N), dtype=torch.float32, device="cuda")
     with pytest.raises(q.QmmError) as ei:
