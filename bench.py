@@ -184,8 +184,13 @@ def recorded_traffic(workload: str):
 
 
 # ---------------------------------------------------------------- GPU arm
-def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, splits=0):
+KERNEL_FLAGS = {"auto": {}, "mma": {}, "tc": {"tcgen05": True}, "simt": {"simt": True}}
+
+
+def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, splits=0,
+                   kernel="auto"):
     spec = synth.SHAPES[shape_name]
+    kf = KERNEL_FLAGS[kernel]
     N, K = spec["N"], spec["K"]
     mats = []
     for r in range(copies):
@@ -193,7 +198,8 @@ def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, s
         if spec["fmt"] == "q4_0":
             blocks = q.quantize_q4_0(w, hadamard=hadamard)
             del w
-            mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=hadamard, k_splits=splits))
+            mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=hadamard, k_splits=splits,
+                                 **kf))
             del blocks
         else:
             codes, scales = q.quantize_fp8(w, hadamard=hadamard)
@@ -239,7 +245,8 @@ def run_gpu(args, ws, rank, local):
                 w = synth.weights_cuda(N, K, 4 * layer + j)
                 blocks = q.quantize_q4_0(w)
                 del w
-                mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, k_splits=args.splits))
+                mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, k_splits=args.splits,
+                                     **KERNEL_FLAGS[args.kernel]))
                 del blocks
         torch.cuda.synchronize()
         Ms = synth.MODEL_MS
@@ -266,7 +273,7 @@ def run_gpu(args, ws, rank, local):
         one = (N * K // 32 * 18) if spec["fmt"] == "q4_0" else (N * K + 4 * (N // 128) * (K // 128))
         copies = args.copies or max(2, -(-4 * L2_BYTES // one))
         mats, spec = build_matrices(q, synth, shape_name, hadamard, copies, torch,
-                                    splits=args.splits)
+                                    splits=args.splits, kernel=args.kernel)
         for M in Ms:
             act = synth.activations_cuda(M, K, spec["seed"] + 1000, outliers=spec["outliers"])
             items = [(m, act, torch.empty((M, N), dtype=torch.float32, device=dev)) for m in mats]
@@ -505,6 +512,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(list(WORKLOADS) + ["model"]), default="q4_attn")
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: >= 4x L2)")
     ap.add_argument("--splits", type=int, default=0, help="force the K split count (0: planner)")
+    ap.add_argument("--kernel", choices=sorted(KERNEL_FLAGS), default="auto",
+                    help="verify kernel: auto (library default: mma.sync), tc (tcgen05, bf16 "
+                         "Q4_0 only), mma (mma.sync), simt (CUDA cores, Q4_0 only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -76,9 +76,11 @@ enum {
   /* Use the CUDA-core (FP32 FMA) verify kernel instead of the tensor-core one.
    * Same results within the tolerance; kept as the measured baseline. */
   QMM_FLAG_SIMT = 1u << 1,
-  /* Q4_0 without rotation: use the warp-level mma.sync kernel instead of the
-   * tcgen05 one (same results within the tolerance; kept for comparison). */
-  QMM_FLAG_MMA_SYNC = 1u << 2
+  /* Q4_0 without rotation: use the tcgen05 kernel (dequantized weights in
+   * tensor memory, one MMA issuer per CTA) instead of the default warp-level
+   * mma.sync kernel.  Same results within the tolerance; slower at M <= 16,
+   * where a 128x16x16 tcgen05 MMA costs about as much as a 128x256x16 one. */
+  QMM_FLAG_TCGEN05 = 1u << 2
 };
 
 /* Description of one weight matrix W[N][K]. */

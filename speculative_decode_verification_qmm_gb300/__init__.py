@@ -16,7 +16,7 @@ import ctypes
 
 from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_ARG,
                    QMM_ERR_M_RANGE, QMM_ERR_SHAPE, QMM_ERR_STATE, QMM_ERR_TIMEOUT,
-                   QMM_FLAG_HADAMARD32, QMM_FLAG_MMA_SYNC, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
+                   QMM_FLAG_HADAMARD32, QMM_FLAG_TCGEN05, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
@@ -27,7 +27,7 @@ __all__ = [
     "QMM_OK", "QMM_ERR_INVALID_ARG", "QMM_ERR_SHAPE", "QMM_ERR_M_RANGE", "QMM_ERR_ALIGN",
     "QMM_ERR_CUDA", "QMM_ERR_TIMEOUT", "QMM_ERR_STATE", "QMM_ERR_DEVICE",
     "QMM_FMT_Q4_0", "QMM_FMT_FP8_E4M3_B128", "QMM_FLAG_HADAMARD32", "QMM_FLAG_SIMT",
-    "QMM_FLAG_MMA_SYNC",
+    "QMM_FLAG_TCGEN05",
 ]
 
 
@@ -187,9 +187,9 @@ class Matrix:
     """One weight matrix on the device, ready for repeated verify calls."""
 
     def __init__(self, fmt: int, weights, N: int, K: int, scales=None, hadamard: bool = False,
-                 simt: bool = False, k_splits: int = 0, stream=None, mma_sync: bool = False):
+                 simt: bool = False, k_splits: int = 0, stream=None, tcgen05: bool = False):
         flags = ((QMM_FLAG_HADAMARD32 if hadamard else 0) | (QMM_FLAG_SIMT if simt else 0)
-                 | (QMM_FLAG_MMA_SYNC if mma_sync else 0))
+                 | (QMM_FLAG_TCGEN05 if tcgen05 else 0))
         self.N, self.K, self.fmt = N, K, fmt
         self.handle = qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream)
 

@@ -24,7 +24,7 @@ QMM_FMT_Q4_0 = 0
 QMM_FMT_FP8_E4M3_B128 = 1
 QMM_FLAG_HADAMARD32 = 1
 QMM_FLAG_SIMT = 2
-QMM_FLAG_MMA_SYNC = 4
+QMM_FLAG_TCGEN05 = 4
 
 
 class qmm_desc(ctypes.Structure):

@@ -44,7 +44,9 @@ struct qmm_handle {
   Plan plan;
   uint8_t* wdev = nullptr;
   size_t wdev_bytes = 0;
-  uint16_t* act_scratch = nullptr;
+  float* f8_scale = nullptr;      // FP8: [n_tiles][S * spc] tile scales
+  uint16_t* act_scratch = nullptr;  // f16 paths: [MAX_M][act_ld]
+  int64_t act_ld = 0;
   size_t act_bytes = 0;
   float* out_scale = nullptr;  // [MAX_M][S]
   int* status = nullptr;       // device error word
@@ -53,12 +55,19 @@ struct qmm_handle {
   float* stage_out = nullptr;     // [MAX_M][N]
   uint64_t wait_limit_ns = DEFAULT_WAIT_LIMIT_NS;
   int last_cuda_error = 0;
-  // tcgen05 path: tensor map over the last activation rows seen (re-encoded
-  // when the pointer, row stride or M changes)
-  CUtensorMap act_map;
-  const void* map_ptr = nullptr;
-  int64_t map_lda = -1;
-  int map_M = -1;
+  // Tensor maps over the activation rows of recent calls, keyed by what they
+  // encode (a graph captures the map by value, so an entry can be reused or
+  // replaced freely).
+  struct MapEntry {
+    const void* ptr = nullptr;
+    int64_t lda = -1;
+    int M = -1, box_r = 0, box_k = 0;
+    bool f16 = false;
+    CUtensorMap map;
+  };
+  static constexpr int MAP_CACHE = 8;
+  MapEntry maps[MAP_CACHE];
+  int map_next = 0;
 };
 
 namespace {
@@ -154,6 +163,7 @@ void free_handle(qmm_handle* h) {
   cudaGetDevice(&old);
   if (old != h->device) cudaSetDevice(h->device);
   cudaFree(h->wdev);
+  cudaFree(h->f8_scale);
   cudaFree(h->act_scratch);
   cudaFree(h->out_scale);
   cudaFree(h->status);
@@ -190,16 +200,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D view of M activation rows for the tcgen05 kernel: dim 0 = 8 consecutive
-// 16-bit values, dim 1 = rows (stride lda), dim 2 = 8-column groups (stride 16
-// bytes); a box of 8 x 16 x 32 lands as [group][row][8 values], the canonical
-// no-swizzle K-major layout, with rows >= M and columns >= K read as zeros.
-cudaError_t encode_act_map(CUtensorMap* map, const void* base, int64_t lda, int M, int64_t K, bool f16) {
+// 3-D view of M activation rows: dim 0 = 8 consecutive 16-bit values, dim 1 =
+// rows (stride lda), dim 2 = 8-column groups (stride 16 bytes).  A box of
+// 8 x box_r x box_k lands as [group][row][8 values] (the canonical no-swizzle
+// K-major layout), with rows >= M and columns >= K read as zeros.
+cudaError_t encode_act_map(CUtensorMap* map, const void* base, int64_t lda, int M, int64_t K, bool f16,
+                           int box_r, int box_k) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t dims[3] = {8, (cuuint64_t)M, (cuuint64_t)((K + 7) / 8)};
   cuuint64_t strides[2] = {(cuuint64_t)lda * 2, 16};
-  cuuint32_t box[3] = {8, 16, 32};
+  cuuint32_t box[3] = {8, (cuuint32_t)box_r, (cuuint32_t)box_k};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -208,22 +219,62 @@ cudaError_t encode_act_map(CUtensorMap* map, const void* base, int64_t lda, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// The verify kernel of the handle's plan.  The tcgen05 kernel reads the
-// caller's bf16 rows through a tensor map, re-encoded when they change.
-cudaError_t launch_verify_kernel(qmm_handle* h, const VerifyParams& vp, const VerifyLaunch& vl,
-                                 const uint16_t* act, int64_t lda, int M) {
-  if (!h->plan.tc) return h->fmt == 0 ? launch_verify_q4(vp, vl) : launch_verify_fp8(vp, vl);
-  if (h->map_ptr != act || h->map_lda != lda || h->map_M != M) {
-    cudaError_t e = encode_act_map(&h->act_map, act, lda, M, h->K, false);
-    if (e != cudaSuccess) {
-      h->map_ptr = nullptr;
-      return e;
+// 2-D view of M activation rows for the mma.sync kernels: dim 0 = K, dim 1 =
+// rows (stride lda); boxes of box_k columns x box_r rows land row after row
+// with the swizzle as wide as a box row (2 x box_k bytes: 128 or 64).
+cudaError_t encode_act_map_2d(CUtensorMap* map, const void* base, int64_t lda, int M, int64_t K,
+                              bool f16, int box_r, int box_k) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_r};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_k * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The tensor map over `rows` (M rows of 16-bit values, stride lda) with the
+// box the handle's kernel loads: the tcgen05 kernel takes a 3-D view, 16 rows
+// x one stage; the mma.sync kernels a 2-D view, R = 8 or 16 rows x one chunk.
+cudaError_t act_map_for(qmm_handle* h, const void* rows, int64_t lda, int M, bool f16,
+                        const CUtensorMap** out) {
+  const int box_r = h->plan.tc ? 16 : (M > 8 ? 16 : 8);
+  const int box_k = h->plan.tc ? Q4_STAGE_K / 8 : h->plan.stage_k / STAGE_CHUNKS;
+  for (auto& m : h->maps)
+    if (m.ptr == rows && m.lda == lda && m.M == M && m.f16 == f16 && m.box_r == box_r &&
+        m.box_k == box_k) {
+      *out = &m.map;
+      return cudaSuccess;
     }
-    h->map_ptr = act;
-    h->map_lda = lda;
-    h->map_M = M;
-  }
-  return launch_verify_tc(vp, &h->act_map, false, vl.ctas, vl.stream);
+  qmm_handle::MapEntry& m = h->maps[h->map_next];
+  h->map_next = (h->map_next + 1) % qmm_handle::MAP_CACHE;
+  m.ptr = nullptr;
+  cudaError_t e = h->plan.tc ? encode_act_map(&m.map, rows, lda, M, h->K, f16, box_r, box_k)
+                             : encode_act_map_2d(&m.map, rows, lda, M, h->K, f16, box_r, box_k);
+  if (e != cudaSuccess) return e;
+  m.ptr = rows;
+  m.lda = lda;
+  m.M = M;
+  m.f16 = f16;
+  m.box_r = box_r;
+  m.box_k = box_k;
+  *out = &m.map;
+  return cudaSuccess;
+}
+
+// The verify kernel of the handle's plan, reading M activation rows of 16-bit
+// values at `rows` (the caller's bf16 rows, or the pre-pass's f16 scratch).
+cudaError_t launch_verify_kernel(qmm_handle* h, const VerifyParams& vp, const VerifyLaunch& vl,
+                                 const void* rows, int64_t lda, int M, bool f16) {
+  const CUtensorMap* map = nullptr;
+  cudaError_t e = act_map_for(h, rows, lda, M, f16, &map);
+  if (e != cudaSuccess) return e;
+  if (h->plan.tc) return launch_verify_tc(vp, map, false, vl.ctas, vl.stream);
+  return h->fmt == 0 ? launch_verify_q4(vp, vl, map) : launch_verify_fp8(vp, vl, map);
 }
 
 }  // namespace
@@ -256,12 +307,16 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   *out = nullptr;
   if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
   if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
-  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_MMA_SYNC))
+  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_TCGEN05))
     return QMM_ERR_INVALID_ARG;
   if (d->k_splits < 0) return QMM_ERR_INVALID_ARG;
   const int fmt = (int)d->format;
   if (fmt == 1 && !d->scales) return QMM_ERR_INVALID_ARG;
   if (fmt == 1 && (d->flags & QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
+  // the tcgen05 kernel serves bf16 Q4_0 only: no rotation, not the CUDA-core baseline
+  if ((d->flags & QMM_FLAG_TCGEN05) &&
+      (fmt != 0 || (d->flags & (QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT))))
+    return QMM_ERR_INVALID_ARG;
   if (d->N < 1 || d->K < 1) return QMM_ERR_SHAPE;
   if (fmt == 0 && d->K % 32) return QMM_ERR_SHAPE;
   if (fmt == 1 && (d->N % 128 || d->K % 128)) return QMM_ERR_SHAPE;
@@ -278,10 +333,9 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   h->flags = d->flags;
   h->N = d->N;
   h->K = d->K;
-  // bf16 Q4_0 runs on the tcgen05 kernel; the f16 paths, the CUDA-core
-  // baseline and QMM_FLAG_MMA_SYNC use the mma.sync kernels.
-  const bool tc = fmt == 0 &&
-                  !(d->flags & (QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_MMA_SYNC));
+  // The mma.sync kernels serve every path; QMM_FLAG_TCGEN05 selects the
+  // tcgen05 kernel for bf16 Q4_0 (checked above).
+  const bool tc = (d->flags & QMM_FLAG_TCGEN05) != 0;
   cudaError_t e = tc ? prepare_tc_attributes()
                      : (fmt == 0 ? prepare_q4_attributes() : prepare_fp8_attributes());
   if (e != cudaSuccess) {
@@ -292,7 +346,8 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   const Plan& p = h->plan;
   const int64_t stages_total = (int64_t)p.S * p.spc;
   h->wdev_bytes = (size_t)p.n_tiles * stages_total * p.stage_bytes;
-  h->act_bytes = (size_t)stages_total * act_stage_bytes(p.stage_k);
+  h->act_ld = stages_total * p.stage_k;
+  h->act_bytes = (size_t)MAX_M * h->act_ld * sizeof(uint16_t);
   h->stage_act_pitch = ceil_div(d->K, 8) * 8;
   void* tmp_w = nullptr;
   void* tmp_s = nullptr;
@@ -310,6 +365,7 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
     ptr = reinterpret_cast<decltype(ptr)>(_p);                  \
   } while (0)
   QMM_ALLOC(h->wdev, h->wdev_bytes);
+  if (fmt == 1) QMM_ALLOC(h->f8_scale, (size_t)p.n_tiles * stages_total * sizeof(float));
   QMM_ALLOC(h->act_scratch, h->act_bytes);
   QMM_ALLOC(h->out_scale, (size_t)MAX_M * p.S * sizeof(float));
   QMM_ALLOC(h->status, sizeof(int));
@@ -334,7 +390,8 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   }
 #undef QMM_ALLOC
   e = p.tc ? launch_repack_tc(wsrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st)
-           : launch_repack(fmt, wsrc, ssrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, st);
+           : launch_repack(fmt, wsrc, ssrc, d->N, d->K, p.n_tiles, p.S, p.spc, h->wdev, h->f8_scale,
+                           st);
   if (e != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->act_scratch, 0, h->act_bytes, st)) != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
@@ -388,6 +445,7 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
     pp.act = act;
     pp.lda = lda;
     pp.out = h->act_scratch;
+    pp.ld_out = h->act_ld;
     pp.out_scale = h->out_scale;
     pp.K = h->K;
     pp.M = M;
@@ -400,9 +458,7 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
 
   VerifyParams vp;
   vp.wdev = h->wdev;
-  vp.act = f16 ? reinterpret_cast<const uint8_t*>(h->act_scratch) : nullptr;
-  vp.act_rows = act;
-  vp.lda = lda;
+  vp.f8_scale = h->f8_scale;
   vp.K = h->K;
   vp.out_scale = f16 ? h->out_scale : nullptr;
   vp.out = out;
@@ -419,7 +475,8 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
   vl.ctas = p.n_tiles * p.S;
   vl.stream = st;
-  e = launch_verify_kernel(h, vp, vl, act, lda, M);
+  e = f16 ? launch_verify_kernel(h, vp, vl, h->act_scratch, h->act_ld, M, true)
+          : launch_verify_kernel(h, vp, vl, act, lda, M, false);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
 }
@@ -502,7 +559,8 @@ int qmm_dequantize(qmm_t h, float* w_out, void* stream) {
   const Plan& p = h->plan;
   cudaError_t e = p.tc ? launch_dequant_tc(h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
                                            (cudaStream_t)stream)
-                       : launch_dequant(h->fmt, h->wdev, h->N, h->K, p.n_tiles, p.S, p.spc, w_out,
+                       : launch_dequant(h->fmt, h->wdev, h->f8_scale, h->N, h->K, p.n_tiles, p.S,
+                                        p.spc, w_out,
                                         (cudaStream_t)stream);
   return e == cudaSuccess ? QMM_OK : cuda_fail(h, e);
 }
@@ -619,6 +677,7 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
     pp.act = act;
     pp.lda = lda;
     pp.out = reinterpret_cast<uint16_t*>(base + act_off);
+    pp.ld_out = h->act_ld;
     pp.out_scale = reinterpret_cast<float*>(base + scale_off);
     pp.K = h->K;
     pp.M = M;
@@ -631,9 +690,7 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
 
   VerifyParams vp;
   vp.wdev = h->wdev;
-  vp.act = f16 ? base + act_off : nullptr;
-  vp.act_rows = act;
-  vp.lda = lda;
+  vp.f8_scale = h->f8_scale;
   vp.K = h->K;
   vp.out_scale = f16 ? reinterpret_cast<const float*>(base + scale_off) : nullptr;
   vp.out = out;
@@ -650,7 +707,8 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
   vl.ctas = p.n_tiles * p.S;
   vl.stream = st;
-  e = launch_verify_kernel(h, vp, vl, act, lda, M);
+  e = f16 ? launch_verify_kernel(h, vp, vl, base + act_off, h->act_ld, M, true)
+          : launch_verify_kernel(h, vp, vl, act, lda, M, false);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
 }

@@ -64,15 +64,11 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t k0 = (int64_t)s * p.spc * p.stage_k;
   const int64_t kr = (int64_t)p.spc * p.stage_k;  // elements of this split
-  const int pitch = p.stage_k + 8;
   const uint16_t* src = p.act + (int64_t)m * p.lda;
   // Earlier kernels may still read the scratch this writes.
   pdl_wait();
 
-  auto dst_index = [&](int64_t kl) -> int64_t {
-    const int64_t st = (int64_t)s * p.spc + kl / p.stage_k;
-    return (st * MAX_M + m) * pitch + (kl % p.stage_k);
-  };
+  auto dst_index = [&](int64_t kl) -> int64_t { return (int64_t)m * p.ld_out + k0 + kl; };
 
   if constexpr (!OUT_F16) {
     for (int64_t kl = (int64_t)tid * 4; kl < kr; kl += 256 * 4) {
@@ -214,7 +210,7 @@ __global__ void repack_q4_kernel(const uint8_t* __restrict__ blocks, int64_t N, 
 
 __global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                                   int64_t N, int64_t K, int S, int spc, int64_t total_units,
-                                  uint8_t* __restrict__ wdev) {
+                                  uint8_t* __restrict__ wdev, float* __restrict__ f8_scale) {
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gt >= total_units * 32) return;
   const int lane = (int)(gt & 31);
@@ -247,10 +243,11 @@ __global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float
   uint8_t* unit = stage + (int64_t)(c * 8 + r) * F8_UNIT_BYTES;
   *reinterpret_cast<uint4*>(unit + 16 * lane) = make_uint4(words[0], words[1], words[2], words[3]);
   if (c == 0 && r == 0 && lane == 0) {
+    // one stage = one 128x128 tile; its scale, indexed [tile][S * spc]
     const int64_t tk_n = K / 128;
     float s = 0.f;
     if (tile * TILE_N < N && kt * 128 < K) s = scales[tile * tk_n + kt];
-    *reinterpret_cast<float4*>(stage + STAGE_CHUNKS * 8 * F8_UNIT_BYTES) = make_float4(s, 0.f, 0.f, 0.f);
+    f8_scale[stage_global] = s;
   }
 }
 
@@ -294,8 +291,9 @@ __global__ void dequant_q4_kernel(const uint8_t* __restrict__ wdev, int64_t N, i
   }
 }
 
-__global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, int64_t N, int64_t K, int S, int spc,
-                                   int64_t total_units, float* __restrict__ out) {
+__global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, const float* __restrict__ f8_scale,
+                                   int64_t N, int64_t K, int S, int spc, int64_t total_units,
+                                   float* __restrict__ out) {
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gt >= total_units * 32) return;
   const int lane = (int)(gt & 31);
@@ -310,7 +308,7 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, int64_t N, 
   const int64_t kbase = ((int64_t)split * spc + i) * F8_STAGE_K + 32 * c;
   const uint8_t* stage = wdev + stage_global * F8_STAGE_BYTES;
   const uint8_t* unit = stage + (int64_t)(c * 8 + r) * F8_UNIT_BYTES;
-  const float s = *reinterpret_cast<const float*>(stage + STAGE_CHUNKS * 8 * F8_UNIT_BYTES);
+  const float s = f8_scale[stage_global];
   const uint4 cw = *reinterpret_cast<const uint4*>(unit + 16 * lane);
   const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -508,26 +506,27 @@ cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int 
 }
 
 cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
-                          int n_tiles, int S, int spc, uint8_t* wdev, cudaStream_t st) {
+                          int n_tiles, int S, int spc, uint8_t* wdev, float* f8_scale,
+                          cudaStream_t st) {
   const int64_t units = (int64_t)n_tiles * S * spc * STAGE_CHUNKS * 8;
   const int64_t threads = units * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)
     repack_q4_kernel<<<blocks, 256, 0, st>>>(wsrc, N, K, S, spc, units, wdev);
   else
-    repack_fp8_kernel<<<blocks, 256, 0, st>>>(wsrc, scales, N, K, S, spc, units, wdev);
+    repack_fp8_kernel<<<blocks, 256, 0, st>>>(wsrc, scales, N, K, S, spc, units, wdev, f8_scale);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(int fmt, const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S,
-                           int spc, float* out, cudaStream_t st) {
+cudaError_t launch_dequant(int fmt, const uint8_t* wdev, const float* f8_scale, int64_t N, int64_t K,
+                           int n_tiles, int S, int spc, float* out, cudaStream_t st) {
   const int64_t units = (int64_t)n_tiles * S * spc * STAGE_CHUNKS * 8;
   const int64_t threads = units * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)
     dequant_q4_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
   else
-    dequant_fp8_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
+    dequant_fp8_kernel<<<blocks, 256, 0, st>>>(wdev, f8_scale, N, K, S, spc, units, out);
   return cudaGetLastError();
 }
 

@@ -9,8 +9,9 @@
 //   number of stages per CTA.  Every stage of every CTA is one contiguous byte
 //   range, so one bulk copy moves it into shared memory:
 //       wdev + ((tile * S + s) * spc + i) * stage_bytes
-//   Inside a stage the bytes are ordered [warp chunk c][row subtile r][unit],
-//   where a unit is what one warp needs for 16 rows x (STAGE_K / 4) columns,
+//   Inside a stage the bytes are ordered [chunk c][row subtile r][unit]: the
+//   four column chunks are contiguous and each is moved by its own bulk copy.
+//   A unit is what one warp needs for 16 rows x (STAGE_K / 4) columns,
 //   already permuted into mma.sync m16n8k16 A-fragment order: lane l (group
 //   g = l / 4, thread t = l % 4) finds its 16 bytes at unit + 16 l.
 //
@@ -26,12 +27,17 @@
 //   FP8 (STAGE_K = 128, chunk = 32 columns):
 //     unit = 512 B codes; lane word v covers k16 step j = v / 2, half h = v % 2;
 //     byte e (0..3) is element row = g + 8 * ((2h + e/2) & 1),
-//     k = 16 j + 2 t + (e & 1) + 8 * ((2h + e/2) >> 1).  The stage ends with a
-//     16-byte record holding the fp32 scale of its 128x128 tile.
+//     k = 16 j + 2 t + (e & 1) + 8 * ((2h + e/2) >> 1).  A stage is exactly one
+//     128x128 weight tile; its fp32 scale lives in a separate array
+//     [tile][stage] next to the stream.
 //
-// Activation scratch: the pre-pass writes the (optionally rotated) activation
-// rows as 16-bit values in the same stage order, [stage][16 rows][ACT_PITCH],
-// with ACT_PITCH = STAGE_K + 8 so that ldmatrix rows fall in distinct banks.
+// Activations reach shared memory through a 2-D tensor map over the 16-bit
+// rows (dim 0: K, dim 1: the M rows).  One box per chunk, CHUNK_K columns x
+// R = 8 or 16 rows, lands as R rows of 2 x CHUNK_K bytes with the map's
+// swizzle of that width, which spreads the eight 16-byte rows of every
+// ldmatrix 8x8 matrix over distinct banks; rows >= M and columns >= K read
+// as zeros.  The f16 paths read the pre-pass's scratch [MAX_M][Kp] the same
+// way.  (The tcgen05 kernel uses a 3-D view instead; see its source.)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -49,16 +55,13 @@ constexpr int MAX_M = 16;
 // Q4_0
 constexpr int Q4_STAGE_K = 256;
 constexpr int Q4_UNIT_BYTES = 576;
-constexpr int Q4_STAGE_BYTES = STAGE_CHUNKS * 8 * Q4_UNIT_BYTES;  // 18432
+constexpr int Q4_CHUNK_BYTES = 8 * Q4_UNIT_BYTES;                 // 4608
+constexpr int Q4_STAGE_BYTES = STAGE_CHUNKS * Q4_CHUNK_BYTES;      // 18432
 // FP8
 constexpr int F8_STAGE_K = 128;
 constexpr int F8_UNIT_BYTES = 512;
-constexpr int F8_STAGE_BYTES = STAGE_CHUNKS * 8 * F8_UNIT_BYTES + 16;  // 16400
-
-__host__ __device__ constexpr int act_pitch(int stage_k) { return stage_k + 8; }
-__host__ __device__ constexpr int act_stage_bytes(int stage_k) {
-  return MAX_M * act_pitch(stage_k) * 2;
-}
+constexpr int F8_CHUNK_BYTES = 8 * F8_UNIT_BYTES;                  // 4096
+constexpr int F8_STAGE_BYTES = STAGE_CHUNKS * F8_CHUNK_BYTES;      // 16384
 
 // Device error word bits (OR-ed into the handle's status word).
 constexpr int DEV_ERR_TIMEOUT_FULL = 1;   // consumer gave up waiting for a stage
@@ -67,10 +70,8 @@ constexpr int DEV_ERR_TIMEOUT_DRAIN = 4;  // copies in flight did not land in ti
 
 struct VerifyParams {
   const uint8_t* wdev;       // repacked weights
-  const uint8_t* act;        // activation scratch (16-bit values, stage order), or NULL
-  const uint16_t* act_rows;  // the caller's bf16 rows (used when act is NULL)
-  int64_t lda;               // row stride of act_rows
-  int64_t K;                 // true K (bytes past it are not copied from act_rows)
+  const float* f8_scale;     // FP8: [n_tiles][S * spc] fp32 scale of each stage's tile
+  int64_t K;                 // true K
   const float* out_scale;    // [MAX_M][S]: multiplier of split s's partial for row m, or NULL
   float* out;                // [M][ldo]
   int* status;               // device error word
@@ -85,7 +86,8 @@ struct VerifyParams {
 struct PrepParams {
   const uint16_t* act;       // caller's bf16 rows
   int64_t lda;
-  uint16_t* out;             // activation scratch
+  uint16_t* out;             // activation scratch [MAX_M][ld_out], 16-bit values
+  int64_t ld_out;            // = S * spc * stage_k
   float* out_scale;          // [MAX_M][S]
   int64_t K;                 // true K
   int M;
@@ -180,6 +182,26 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// Tiled tensor copies global -> shared of one box of a 2-D or 3-D tensor map
+// (coordinates innermost first).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -264,9 +286,19 @@ struct Bf16Op {
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
           "f"(c[3]));
   }
-  // 4 pairs from one 32-bit word of 8 nibbles: pair p from nibbles (p, p + 4).
-  // bf16 128.0 = 0x4300 has a 7-bit mantissa whose low 4 bits take q exactly;
-  // subtracting 136 = 0x4308 leaves q - 8.
+  // Offset form: 4 pairs of 128 + q (exact) from one 32-bit word of 8 nibbles,
+  // pair p from nibbles (p, p + 4), one lop3 per pair; the kernel adds
+  // -136 * sum(a) through the MMA's accumulator input instead of subtracting
+  // 136 from every weight.
+  __device__ __forceinline__ static void biased_word(uint32_t w, uint32_t (&r)[4]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+      asm("lop3.b32 %0, %1, %2, %3, 0xEA;"
+          : "=r"(r[p])
+          : "r"(w >> (4 * p)), "r"(0x000F000Fu), "r"(0x43004300u));
+  }
+  // The same pairs as q - 8: bf16 128.0 = 0x4300 has a 7-bit mantissa whose
+  // low 4 bits take q exactly; subtracting 136 = 0x4308 leaves q - 8.
   __device__ __forceinline__ static void dequant_word(uint32_t w, uint32_t (&r)[4]) {
     const uint32_t magic = 0x43004300u, bias = 0x43084308u;
 #pragma unroll

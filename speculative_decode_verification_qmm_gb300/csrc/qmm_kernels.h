@@ -43,16 +43,20 @@ cudaError_t launch_repack_tc(const uint8_t* blocks, int64_t N, int64_t K, int n_
 cudaError_t launch_dequant_tc(const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S, int spc,
                               float* out, cudaStream_t st);
 
-cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l);
-cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l);
+// act_map points to a CUtensorMap over the activation rows (see qmm_common.cuh)
+// with boxes of 8 values x R rows x chunk columns / 8, R = 8 for M <= 8, else 16.
+cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
+cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
 
 cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStream_t st);
 cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int M, int64_t K,
                               int sm_count, cudaStream_t st);
+// FP8: f8_scale receives [n_tiles][S * spc] tile scales (zero past N or K).
 cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
-                          int n_tiles, int S, int spc, uint8_t* wdev, cudaStream_t st);
-cudaError_t launch_dequant(int fmt, const uint8_t* wdev, int64_t N, int64_t K, int n_tiles, int S,
-                           int spc, float* out, cudaStream_t st);
+                          int n_tiles, int S, int spc, uint8_t* wdev, float* f8_scale,
+                          cudaStream_t st);
+cudaError_t launch_dequant(int fmt, const uint8_t* wdev, const float* f8_scale, int64_t N, int64_t K,
+                           int n_tiles, int S, int spc, float* out, cudaStream_t st);
 cudaError_t launch_quantize_q4(const float* w, int64_t N, int64_t K, int had, uint8_t* blocks,
                                cudaStream_t st);
 cudaError_t launch_quantize_fp8(const float* w, int64_t N, int64_t K, int had, uint8_t* codes,

@@ -1,26 +1,28 @@
 // qmm_verify.cuh -- the weight-streaming verify kernel.
 //
-// One CTA = one row tile of W (128 rows) x one K split.  A producer warp
-// streams the CTA's stages through an NS-deep shared-memory ring guarded by
-// mbarriers: per stage one bulk copy of the repacked weights and one bulk copy
-// per drafted row of the activations (straight from the caller's bf16 rows, or
-// from the pre-pass scratch on the f16 paths).  Eight compute warps split every
-// stage into four column chunks x two halves of the tile's rows; each warp
-// dequantizes its codes in registers straight into mma.sync A fragments
-// (weights are the MMA's M dimension, drafted rows its N = 8 or 16 dimension,
-// "swap AB"), keeps fp32 accumulators in registers across the CTA's K range,
-// and applies the per-block (Q4_0) or per-tile (FP8) scale with packed fp32
-// FMAs.  The epilogue adds the four chunk partials in a fixed order through
-// shared memory, multiplies by the pre-pass's per-(row, split) power-of-two
-// factor, and either writes `out` (one split) or, when the K range is split,
-// leaves its partial in shared memory: the S CTAs of a row tile form one
-// thread-block cluster and each adds a slice of the tile's rows over the S
-// partials through distributed shared memory, in split order (deterministic,
-// no global scratch, no atomics).
+// One CTA = one row tile of W (128 rows) x one K split.  A producer thread
+// streams the CTA's stages through an NS-deep shared-memory ring.  A stage is
+// four column chunks and each chunk has its own full/empty mbarrier pair: one
+// bulk copy of the chunk's repacked weights and one tensor-map box of the
+// activations (R = 8 or 16 drafted rows x the chunk's columns) complete its
+// full barrier.  Eight compute warps (chunk x half of the tile's rows) wait for
+// their own chunk only, dequantize their codes in registers straight into
+// mma.sync A fragments (weights are the MMA's M dimension, drafted rows its
+// N = 8 or 16 dimension, "swap AB"), keep fp32 accumulators in registers
+// across the CTA's K range, and apply the per-block (Q4_0) or per-tile (FP8)
+// scale with packed fp32 FMAs.  The epilogue adds the four chunk partials in a
+// fixed order through shared memory, multiplies by the pre-pass's per-(row,
+// split) power-of-two factor, and either writes `out` (one split) or, when the
+// K range is split, leaves its partial in shared memory: the S CTAs of a row
+// tile form one thread-block cluster and each adds a slice of the tile's rows
+// over the S partials through distributed shared memory, in split order
+// (deterministic, no global scratch, no atomics).
 //
 // The summation order of every output element is fixed by (N, K, plan) and
 // never depends on M, so row m of the result is bit-identical for M = 1..16.
 #pragma once
+
+#include <cuda.h>
 
 #include <type_traits>
 
@@ -35,6 +37,7 @@ template <>
 struct FmtTraits<0> {  // Q4_0
   static constexpr int STAGE_K = Q4_STAGE_K;
   static constexpr int STAGE_BYTES = Q4_STAGE_BYTES;
+  static constexpr int CHUNK_BYTES = Q4_CHUNK_BYTES;
   static constexpr int UNIT_BYTES = Q4_UNIT_BYTES;
   static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 64
 };
@@ -43,6 +46,7 @@ template <>
 struct FmtTraits<1> {  // FP8 E4M3, 128x128 scales
   static constexpr int STAGE_K = F8_STAGE_K;
   static constexpr int STAGE_BYTES = F8_STAGE_BYTES;
+  static constexpr int CHUNK_BYTES = F8_CHUNK_BYTES;
   static constexpr int UNIT_BYTES = F8_UNIT_BYTES;
   static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 32
 };
@@ -52,15 +56,20 @@ struct FmtTraits<1> {  // FP8 E4M3, 128x128 scales
 constexpr int WARP_SUBTILES = 8 * STAGE_CHUNKS / COMPUTE_WARPS;  // 4
 static_assert(WARP_SUBTILES * 2 == 8, "two row halves per chunk");
 
-template <int FMT, int NS>
+// R = activation rows staged per chunk (8 for M <= 8, else 16).  Offsets are
+// from the dynamic shared memory base rounded up to 1024 bytes (BYTES
+// includes that slack), the period of the tensor map's swizzle.
+template <int FMT, int NS, int R>
 struct SmemLayout {
   using F = FmtTraits<FMT>;
   static constexpr int W_OFF = 0;
   static constexpr int A_OFF = NS * F::STAGE_BYTES;
-  static constexpr int A_BYTES = NS * act_stage_bytes(F::STAGE_K);
-  static constexpr int BAR_OFF = A_OFF + A_BYTES;
-  static constexpr int FLAG_OFF = BAR_OFF + 2 * NS * 8;
-  static constexpr int BYTES = FLAG_OFF + 16;
+  static constexpr int A_CHUNK = F::CHUNK_K * R * 2;  // one tensor-map box: R rows x CHUNK_K
+  static constexpr int A_STAGE = STAGE_CHUNKS * A_CHUNK;
+  static constexpr int A_BYTES = NS * A_STAGE;
+  static constexpr int BAR_OFF = A_OFF + A_BYTES;  // full[NS][4], then empty[NS][4]
+  static constexpr int FLAG_OFF = BAR_OFF + 2 * NS * STAGE_CHUNKS * 8;
+  static constexpr int BYTES = FLAG_OFF + 16 + 1024;
   // epilogue areas (reuse the weight ring): chunk partials [chunk][row][RED_PITCH],
   // then the CTA partial read by the cluster [row][CP_PITCH]
   static constexpr int RED_PITCH = MAX_M + 2;  // floats per row
@@ -69,7 +78,9 @@ struct SmemLayout {
   static constexpr int CP_OFF = RED_BYTES;
   static constexpr int CP_BYTES = TILE_N * CP_PITCH * 4;
   static_assert(CP_OFF + CP_BYTES <= NS * F::STAGE_BYTES, "epilogue areas must fit in the ring");
-  static_assert(A_OFF % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
+  static_assert(A_OFF % 1024 == 0 && A_CHUNK % (F::CHUNK_K * 2 * 8) == 0,
+                "every box starts on a swizzle period");
+  static_assert(F::CHUNK_BYTES % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
 };
 
 // e4m3 pair (16 bits) -> f16x2, exact.
@@ -81,16 +92,40 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
   return r;
 }
 
-// B fragments for NSTEP k16 steps of the activation chunk at `abase`:
-// b[s][0..1] serve draft rows 0..7, b[s][2..3] rows 8..15.
-template <int NSTEP, int STAGE_K>
+// Shared-memory address of the 8 values k = 8 kc .. 8 kc + 7 of activation
+// row `row` in a chunk box: rows of RB = 2 x CHUNK_K bytes, and the tensor
+// map's RB-byte swizzle moves 16-byte piece kc of row r to kc ^ (r & 7)
+// (128-byte rows) or kc ^ ((r >> 1) & 3) (64-byte rows).  Box bases are
+// aligned to the swizzle period, so row r's pattern depends on r alone.
+template <int RB>
+__device__ __forceinline__ uint32_t act_piece(uint32_t abase, int row, int kc) {
+  static_assert(RB == 128 || RB == 64, "swizzle width");
+  const int sw = RB == 128 ? (row & 7) : ((row >> 1) & 3);
+  return abase + (uint32_t)(row * RB + ((kc ^ sw) << 4));
+}
+
+// B fragments for the NSTEP k16 steps of the activation chunk at `abase` (R
+// rows of RB bytes): b[s][0..1] serve draft rows 0..7, b[s][2..3] rows 8..15
+// (R = 16 only).
+template <int NSTEP, int R, int RB>
 __device__ __forceinline__ void load_b_frags(uint32_t abase, int lane, uint32_t (&b)[NSTEP][4]) {
-  const int row = (lane & 7) + ((lane >> 4) << 3);
-  const int koff = ((lane >> 3) & 1) * 8;
+  static_assert(NSTEP % 2 == 0, "pairs of k16 steps");
+  if constexpr (R == 16) {
+    // matrices: rows 0-7 / 8-15 x columns 0-7 / 8-15 of step s
+    const int row = (lane & 7) + ((lane >> 4) << 3);
+    const int kh = (lane >> 3) & 1;
 #pragma unroll
-  for (int s = 0; s < NSTEP; ++s) {
-    const uint32_t addr = abase + (uint32_t)(row * act_pitch(STAGE_K) + s * 16 + koff) * 2u;
-    ldmatrix_x4(addr, b[s][0], b[s][1], b[s][2], b[s][3]);
+    for (int s = 0; s < NSTEP; ++s)
+      ldmatrix_x4(act_piece<RB>(abase, row, 2 * s + kh), b[s][0], b[s][1], b[s][2], b[s][3]);
+  } else {
+    // matrices: columns 0-7 / 8-15 of steps s and s + 1
+    const int row = lane & 7;
+    const int kq = lane >> 3;
+#pragma unroll
+    for (int s = 0; s < NSTEP; s += 2) {
+      ldmatrix_x4(act_piece<RB>(abase, row, 2 * s + kq), b[s][0], b[s][1], b[s + 1][0], b[s + 1][1]);
+      b[s][2] = b[s][3] = b[s + 1][2] = b[s + 1][3] = 0u;
+    }
   }
 }
 
@@ -103,8 +138,27 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
                                              float (&acc)[WARP_SUBTILES][2][4]) {
   const int g = lane >> 2;
   uint32_t b[4][4];
-  load_b_frags<4, Q4_STAGE_K>(abase, lane, b);
-  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  load_b_frags<4, 8 * NT8, 2 * Q4_STAGE_K / STAGE_CHUNKS>(abase, lane, b);
+  // bf16: the weights enter the MMA as 128 + q and every block's accumulator
+  // starts at -136 * sum_k a[m][k] (an MMA with a constant A operand), so the
+  // block sum is sum (q - 8) a without a subtraction per weight.  f16: the
+  // dequantizer returns q - 8 itself and the blocks start at zero.
+  constexpr bool FOLD = std::is_same<Op, Bf16Op>::value;
+  float c0[2][NT8][4];
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c0[blk][j][e] = 0.f;
+      if constexpr (FOLD) {
+        constexpr uint32_t kNeg136 = 0xC308C308u;  // bf16x2 (-136, -136)
+        Op::mma(c0[blk][j], kNeg136, kNeg136, kNeg136, kNeg136, b[2 * blk][2 * j],
+                b[2 * blk][2 * j + 1], c0[blk][j]);
+        Op::mma(c0[blk][j], kNeg136, kNeg136, kNeg136, kNeg136, b[2 * blk + 1][2 * j],
+                b[2 * blk + 1][2 * j + 1], c0[blk][j]);
+      }
+    }
 #pragma unroll
   for (int r = 0; r < WARP_SUBTILES; ++r) {
     const uint32_t unit = wunit0 + (uint32_t)(r * Q4_UNIT_BYTES);
@@ -114,15 +168,20 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       uint32_t a0[4], a1[4];
-      Op::dequant_word(words[2 * blk + 0], a0);
-      Op::dequant_word(words[2 * blk + 1], a1);
+      if constexpr (FOLD) {
+        Bf16Op::biased_word(words[2 * blk + 0], a0);
+        Bf16Op::biased_word(words[2 * blk + 1], a1);
+      } else {
+        Op::dequant_word(words[2 * blk + 0], a0);
+        Op::dequant_word(words[2 * blk + 1], a1);
+      }
       const uint32_t dpair = blk ? sc.y : sc.x;  // (d[g], d[g+8]) of this block
       const float dg = __half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF)));
       const float dg8 = __half2float(__ushort_as_half((unsigned short)(dpair >> 16)));
 #pragma unroll
       for (int j = 0; j < NT8; ++j) {
         float pp[4];
-        Op::mma(pp, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], zero);
+        Op::mma(pp, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], c0[blk][j]);
         Op::mma(pp, a1[0], a1[1], a1[2], a1[3], b[2 * blk + 1][2 * j], b[2 * blk + 1][2 * j + 1], pp);
         ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
         ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);
@@ -135,7 +194,7 @@ template <int NT8>
 __device__ __forceinline__ void f8_stage_mma(uint32_t wunit0, uint32_t abase, float s, int lane,
                                              float (&acc)[WARP_SUBTILES][2][4]) {
   uint32_t b[2][4];
-  load_b_frags<2, F8_STAGE_K>(abase, lane, b);
+  load_b_frags<2, 8 * NT8, 2 * F8_STAGE_K / STAGE_CHUNKS>(abase, lane, b);
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int r = 0; r < WARP_SUBTILES; ++r) {
@@ -159,56 +218,53 @@ __device__ __forceinline__ void f8_stage_mma(uint32_t wunit0, uint32_t abase, fl
 // CUDA-core baseline for Q4_0: fp32 dequantization and one FMA per weight and
 // drafted row; each lane accumulates its own columns and the four lanes of a
 // group are added with warp shuffles at the end (split K inside the warp).
-// Warp w owns row subtile w over all four chunks of every stage.
+// Warp w owns row subtile w over all four chunks of every stage; this is one
+// chunk (its unit at `unit`, the chunk's activation box at `achunk`).
 template <typename T, int NT8>
-__device__ __forceinline__ void q4_stage_simt(uint32_t wstage, uint32_t astage, int warp, int lane,
-                                              int M, float (&acc)[2][MAX_M]) {
+__device__ __forceinline__ void q4_chunk_simt(uint32_t unit, uint32_t achunk, int lane, int M,
+                                              float (&acc)[2][MAX_M]) {
   const int g = lane >> 2, t = lane & 3;
   constexpr int MR = 8 * NT8;
-#pragma unroll 1
-  for (int c = 0; c < STAGE_CHUNKS; ++c) {
-    const uint32_t unit = wstage + (uint32_t)((c * 8 + warp) * Q4_UNIT_BYTES);
-    const uint4 codes = lds128(unit + 16u * lane);
-    const uint2 sc = lds64(unit + 512u + 8u * g);
-    const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+  const uint4 codes = lds128(unit + 16u * lane);
+  const uint2 sc = lds64(unit + 512u + 8u * g);
+  const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      const uint32_t dpair = blk ? sc.y : sc.x;
-      const float d[2] = {__half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF))),
-                          __half2float(__ushort_as_half((unsigned short)(dpair >> 16)))};
-      float part[2][MR];
+  for (int blk = 0; blk < 2; ++blk) {
+    const uint32_t dpair = blk ? sc.y : sc.x;
+    const float d[2] = {__half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF))),
+                        __half2float(__ushort_as_half((unsigned short)(dpair >> 16)))};
+    float part[2][MR];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int m = 0; m < MR; ++m) part[h][m] = 0.f;
+      for (int m = 0; m < MR; ++m) part[h][m] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t w = words[2 * blk + j];
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t w = words[2 * blk + j];
 #pragma unroll
-        for (int pn = 0; pn < 8; ++pn) {
-          const int pair = pn & 3, half = pn >> 2;
-          const int h = pair & 1;  // row g or g + 8
-          const int k = c * 64 + 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);
-          const float qv = __int_as_float(0x4B000000 | ((w >> (4 * pn)) & 15u)) - 8388616.0f;
+      for (int pn = 0; pn < 8; ++pn) {
+        const int pair = pn & 3, half = pn >> 2;
+        const int h = pair & 1;  // row g or g + 8
+        const int k = 32 * blk + 16 * j + 2 * t + half + 8 * (pair >> 1);  // column in the chunk
+        const float qv = __int_as_float(0x4B000000 | ((w >> (4 * pn)) & 15u)) - 8388616.0f;
 #pragma unroll
-          for (int m = 0; m < MR; ++m) {
-            if (m < M) {
-              const uint32_t bits = lds_u16(astage + (uint32_t)(m * act_pitch(Q4_STAGE_K) + k) * 2u);
-              float a;
-              if constexpr (std::is_same<T, __nv_bfloat16>::value)
-                a = __uint_as_float(bits << 16);
-              else
-                a = __half2float(__ushort_as_half((unsigned short)bits));
-              part[h][m] = fmaf(qv, a, part[h][m]);
-            }
+        for (int m = 0; m < MR; ++m) {
+          if (m < M) {
+            const uint32_t bits = lds_u16(act_piece<128>(achunk, m, k >> 3) + (uint32_t)(k & 7) * 2u);
+            float a;
+            if constexpr (std::is_same<T, __nv_bfloat16>::value)
+              a = __uint_as_float(bits << 16);
+            else
+              a = __half2float(__ushort_as_half((unsigned short)bits));
+            part[h][m] = fmaf(qv, a, part[h][m]);
           }
         }
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int m = 0; m < MR; ++m) acc[h][m] = fmaf(d[h], part[h][m], acc[h][m]);
     }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int m = 0; m < MR; ++m) acc[h][m] = fmaf(d[h], part[h][m], acc[h][m]);
   }
 }
 
@@ -216,45 +272,52 @@ __device__ __forceinline__ void q4_stage_simt(uint32_t wstage, uint32_t astage, 
 // The kernel.
 //   FMT  0 = Q4_0, 1 = FP8
 //   Op   Bf16Op or F16Op (FP8 always F16Op)
-//   NT8  1 for M <= 8, 2 for M <= 16
+//   NT8  1 for M <= 8, 2 for M <= 16 (R = 8 * NT8 activation rows staged)
 //   SIMT true: CUDA-core baseline compute (Q4_0 only)
-//   NS   pipeline depth
+//   NS   pipeline depth in stages
+// `amap` is a 2-D tensor map over the 16-bit activation rows (see
+// qmm_common.cuh) whose boxes are CHUNK_K columns x R rows, swizzled by
+// 2 x CHUNK_K bytes.
 // ---------------------------------------------------------------------------
+// Two CTAs per SM: 18 warps need at most 5 warps' registers per SM
+// sub-partition, i.e. 96 registers per thread.
 template <int FMT, typename Op, int NT8, bool SIMT, int NS>
-__global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constant__ VerifyParams p) {
+__global__ void __launch_bounds__(THREADS, 2)
+    verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap amap) {
   using F = FmtTraits<FMT>;
-  using L = SmemLayout<FMT, NS>;
-  constexpr int PITCH_B = act_pitch(F::STAGE_K) * 2;  // bytes per activation row in shared memory
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int R = 8 * NT8;
+  using L = SmemLayout<FMT, NS, R>;
+  constexpr int NCH = STAGE_CHUNKS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x / p.S;
   const int split = blockIdx.x % p.S;
   const int M = p.M;
 
-  const uint32_t s_base = smem_u32(smem);
+  const uint32_t s_raw = smem_u32(smem_raw);
+  const uint32_t s_base = (s_raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (s_base - s_raw);
   const uint32_t s_w = s_base + L::W_OFF;
   const uint32_t s_a = s_base + L::A_OFF;
-  const uint32_t s_full = s_base + L::BAR_OFF;
-  const uint32_t s_empty = s_full + NS * 8;
-  // [0] abort, [1] this CTA adds the split partials, [2] stages issued by the producer
+  const uint32_t s_full = s_base + L::BAR_OFF;        // [slot][chunk]
+  const uint32_t s_empty = s_full + NS * NCH * 8;     // [slot][chunk]
+  auto full_bar = [&](int slot, int c) { return s_full + (uint32_t)(slot * NCH + c) * 8u; };
+  auto empty_bar = [&](int slot, int c) { return s_empty + (uint32_t)(slot * NCH + c) * 8u; };
+  // [0] abort, [2] chunk copies issued by the producer
   volatile int* s_flag = reinterpret_cast<volatile int*>(smem + L::FLAG_OFF);
 
-  // Zero the activation ring: rows >= M are never copied, and in the last
-  // stage the columns past K must hold finite values (their weights are 0).
-  for (int i = tid * 16; i < L::A_BYTES; i += THREADS * 16)
-    *reinterpret_cast<uint4*>(smem + L::A_OFF + i) = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < NS * NCH; ++i) {
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_empty + 8 * i, COMPUTE_WARPS);
+      // MMA warps: two per chunk; CUDA-core warps: every warp reads every chunk
+      mbar_init(s_empty + 8 * i, SIMT ? COMPUTE_WARPS : COMPUTE_WARPS / NCH);
     }
     s_flag[0] = 0;
     s_flag[1] = 0;
     s_flag[2] = 0;
     fence_mbar_init();
   }
-  fence_proxy_async_smem();
   __syncthreads();
   // Let the next kernel in the stream start its prologue (weight prefetch).
   pdl_trigger();
@@ -262,69 +325,52 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
   const int nst = p.spc;
   const int64_t gstage0 = (int64_t)split * nst;  // global index of this CTA's first stage
   const uint8_t* wsrc = p.wdev + ((size_t)tile * p.S + split) * nst * F::STAGE_BYTES;
-  const bool direct = (p.act == nullptr);
-  // activation bytes per drafted row for stage i, and the source of row m
-  auto row_bytes = [&](int i) -> uint32_t {
-    if (!direct) return (uint32_t)(F::STAGE_K * 2);
-    const int64_t k0 = (gstage0 + i) * F::STAGE_K;
-    int64_t v = p.K - k0;
-    v = v < 0 ? 0 : (v > F::STAGE_K ? F::STAGE_K : v);
-    return (uint32_t)(v * 2);
-  };
-  auto row_src = [&](int i, int m) -> const void* {
-    if (direct) return p.act_rows + (int64_t)m * p.lda + (gstage0 + i) * F::STAGE_K;
-    return p.act + (size_t)(gstage0 + i) * act_stage_bytes(F::STAGE_K) + (size_t)m * PITCH_B;
-  };
+  const int k0 = (int)(gstage0 * F::STAGE_K);  // first column of this CTA (a multiple of 8)
+  constexpr uint32_t CHUNK_TX = F::CHUNK_BYTES + L::A_CHUNK;
 
   if (warp == COMPUTE_WARPS) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol = policy_evict_first();
-    const int pre = nst < NS ? nst : NS;
-    // Weights never depend on earlier kernels: fetch the first stages now.
     if (lane == 0) {
-      for (int i = 0; i < pre; ++i) {
-        mbar_expect_tx(s_full + 8 * i, F::STAGE_BYTES);
-        bulk_g2s_hint(s_w + i * F::STAGE_BYTES, wsrc + (size_t)i * F::STAGE_BYTES, F::STAGE_BYTES,
-                      s_full + 8 * i, pol);
-      }
-    }
-    // Activations may be written by the previous kernel: wait for it.
-    pdl_wait();
-    for (int i = 0; i < pre; ++i) {
-      const uint32_t rb = row_bytes(i);
-      if (lane == 0) mbar_arrive_expect_tx(s_full + 8 * i, rb * (uint32_t)M);
-      __syncwarp();
-      if (lane < M && rb)
-        bulk_g2s(s_a + i * act_stage_bytes(F::STAGE_K) + lane * PITCH_B, row_src(i, lane), rb,
-                 s_full + 8 * i);
-    }
-    int issued = pre;
-    for (int i = NS; i < nst; ++i) {
-      const int slot = i % NS;
-      int ok = 0;
-      if (lane == 0) {
-        ok = mbar_wait_bounded(s_empty + 8 * slot, ((i / NS) - 1) & 1, p.wait_limit_ns) ? 1 : 0;
-        if (!ok) {
-          atomicOr(p.status, DEV_ERR_TIMEOUT_EMPTY);
-          s_flag[0] = 1;
+      const uint64_t pol = policy_evict_first();
+      const int pre = nst < NS ? nst : NS;
+      // Weights never depend on earlier kernels: fetch the first stages now.
+      for (int i = 0; i < pre; ++i)
+        for (int c = 0; c < NCH; ++c) {
+          mbar_arrive_expect_tx(full_bar(i, c), CHUNK_TX);
+          bulk_g2s_hint(s_w + i * F::STAGE_BYTES + c * F::CHUNK_BYTES,
+                        wsrc + (size_t)i * F::STAGE_BYTES + c * F::CHUNK_BYTES, F::CHUNK_BYTES,
+                        full_bar(i, c), pol);
         }
-        ok = ok && !s_flag[0];
+      // Activations may be written by the previous kernel: wait for it.
+      pdl_wait();
+      for (int i = 0; i < pre; ++i)
+        for (int c = 0; c < NCH; ++c)
+          tma_load_2d(s_a + i * L::A_STAGE + c * L::A_CHUNK, &amap,
+                      k0 + i * F::STAGE_K + c * F::CHUNK_K, 0, full_bar(i, c));
+      int issued = pre * NCH;
+      bool ok = true;
+      for (int i = NS; i < nst && ok; ++i) {
+        const int slot = i % NS;
+        for (int c = 0; c < NCH; ++c) {
+          if (!mbar_wait_bounded(empty_bar(slot, c), ((i / NS) - 1) & 1, p.wait_limit_ns)) {
+            atomicOr(p.status, DEV_ERR_TIMEOUT_EMPTY);
+            s_flag[0] = 1;
+          }
+          if (s_flag[0]) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(slot, c), CHUNK_TX);
+          bulk_g2s_hint(s_w + slot * F::STAGE_BYTES + c * F::CHUNK_BYTES,
+                        wsrc + (size_t)i * F::STAGE_BYTES + c * F::CHUNK_BYTES, F::CHUNK_BYTES,
+                        full_bar(slot, c), pol);
+          tma_load_2d(s_a + slot * L::A_STAGE + c * L::A_CHUNK, &amap,
+                      k0 + i * F::STAGE_K + c * F::CHUNK_K, 0, full_bar(slot, c));
+          ++issued;
+        }
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
-      const uint32_t rb = row_bytes(i);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(s_full + 8 * slot, F::STAGE_BYTES + rb * (uint32_t)M);
-        bulk_g2s_hint(s_w + slot * F::STAGE_BYTES, wsrc + (size_t)i * F::STAGE_BYTES,
-                      F::STAGE_BYTES, s_full + 8 * slot, pol);
-      }
-      __syncwarp();
-      if (lane < M && rb)
-        bulk_g2s(s_a + slot * act_stage_bytes(F::STAGE_K) + lane * PITCH_B, row_src(i, lane), rb,
-                 s_full + 8 * slot);
-      issued = i + 1;
+      s_flag[2] = issued;
     }
-    if (lane == 0) s_flag[2] = issued;
   }
 
   // Accumulators (registers) of the compute warps.
@@ -344,49 +390,69 @@ __global__ void __launch_bounds__(THREADS, 2) verify_kernel(const __grid_constan
       for (int m = 0; m < MAX_M; ++m) accs[h][m] = 0.f;
   }
 
-  const int chunk = warp & (STAGE_CHUNKS - 1);
-  const int sub0 = (warp / STAGE_CHUNKS) * WARP_SUBTILES;  // first row subtile of this warp
+  const int chunk = warp & (NCH - 1);
+  const int sub0 = (warp / NCH) * WARP_SUBTILES;  // first row subtile of this warp
   if (warp < COMPUTE_WARPS) {
     // ------------------------------------------------------------ compute
-    for (int i = 0; i < nst; ++i) {
-      const int slot = i % NS;
-      if (!mbar_wait_bounded(s_full + 8 * slot, (i / NS) & 1, p.wait_limit_ns)) {
-        if (lane == 0) atomicOr(p.status, DEV_ERR_TIMEOUT_FULL);
-        s_flag[0] = 1;
-        break;
-      }
-      const uint32_t wst = s_w + slot * F::STAGE_BYTES;
-      const uint32_t ast = s_a + slot * act_stage_bytes(F::STAGE_K);
-      if constexpr (FMT == 0) {
-        if constexpr (SIMT) {
-          q4_stage_simt<typename std::conditional<std::is_same<Op, Bf16Op>::value, __nv_bfloat16,
-                                                  __half>::type,
-                        NT8>(wst, ast, warp, lane, M, accs);
-        } else {
-          q4_stage_mma<Op, NT8>(wst + (chunk * 8 + sub0) * Q4_UNIT_BYTES,
-                                ast + chunk * F::CHUNK_K * 2, lane, acc);
+    if constexpr (!SIMT) {
+      const float* f8s = FMT == 1 ? p.f8_scale + (size_t)tile * p.S * nst + gstage0 : nullptr;
+      for (int i = 0; i < nst; ++i) {
+        const int slot = i % NS;
+        float fs = 0.f;
+        if constexpr (FMT == 1) fs = __ldg(f8s + i);  // lands while the chunk is awaited
+        if (!mbar_wait_bounded(full_bar(slot, chunk), (i / NS) & 1, p.wait_limit_ns)) {
+          if (lane == 0) atomicOr(p.status, DEV_ERR_TIMEOUT_FULL);
+          s_flag[0] = 1;
+          break;
         }
-      } else {
-        const float s = lds_f32(wst + (F::STAGE_BYTES - 16));
-        f8_stage_mma<NT8>(wst + (chunk * 8 + sub0) * F8_UNIT_BYTES, ast + chunk * F::CHUNK_K * 2,
-                          s, lane, acc);
+        const uint32_t wch = s_w + slot * F::STAGE_BYTES + chunk * F::CHUNK_BYTES +
+                             sub0 * F::UNIT_BYTES;
+        const uint32_t ach = s_a + slot * L::A_STAGE + chunk * L::A_CHUNK;
+        if constexpr (FMT == 0)
+          q4_stage_mma<Op, NT8>(wch, ach, lane, acc);
+        else
+          f8_stage_mma<NT8>(wch, ach, fs, lane, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(slot, chunk));
+        if (s_flag[0]) break;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty + 8 * slot);
-      if (s_flag[0]) break;
+    } else {
+      using T = typename std::conditional<std::is_same<Op, Bf16Op>::value, __nv_bfloat16,
+                                          __half>::type;
+      bool ok = true;
+      for (int i = 0; i < nst && ok; ++i) {
+        const int slot = i % NS;
+#pragma unroll 1
+        for (int c = 0; c < NCH; ++c) {
+          if (!mbar_wait_bounded(full_bar(slot, c), (i / NS) & 1, p.wait_limit_ns)) {
+            if (lane == 0) atomicOr(p.status, DEV_ERR_TIMEOUT_FULL);
+            s_flag[0] = 1;
+            ok = false;
+            break;
+          }
+          q4_chunk_simt<T, NT8>(s_w + slot * F::STAGE_BYTES + c * F::CHUNK_BYTES +
+                                    warp * F::UNIT_BYTES,
+                                s_a + slot * L::A_STAGE + c * L::A_CHUNK, lane, M, accs);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(slot, c));
+        }
+        if (s_flag[0]) ok = false;
+      }
     }
   }
   __syncthreads();
   const bool aborted = s_flag[0] != 0;
   if (aborted) {
     // Give up: no copy issued by this CTA may still be landing in shared memory
-    // when the CTA exits.  Only the last NS issued stages can be in flight, and
-    // each of them is the latest phase armed on its slot; its phase completes
-    // when its bytes land, whether or not a compute warp waited for it.
+    // when the CTA exits.  Only the chunks of the last NS issued stages can be
+    // in flight, and each of them is the latest phase armed on its barrier;
+    // that phase completes when its bytes land, whether or not a compute warp
+    // waited for it.
     if (warp == COMPUTE_WARPS && lane == 0) {
       const int issued = s_flag[2];
-      for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i) {
-        if (!mbar_wait_bounded(s_full + 8 * (i % NS), (i / NS) & 1, 1000000000ull))
+      for (int x = issued - NS * NCH < 0 ? 0 : issued - NS * NCH; x < issued; ++x) {
+        const int i = x / NCH, c = x % NCH;
+        if (!mbar_wait_bounded(full_bar(i % NS, c), (i / NS) & 1, 1000000000ull))
           atomicOr(p.status, DEV_ERR_TIMEOUT_DRAIN);
       }
     }

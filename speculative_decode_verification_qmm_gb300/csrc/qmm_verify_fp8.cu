@@ -8,11 +8,11 @@ namespace {
 constexpr int NS_F8 = 5;
 
 template <int NT8>
-cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l) {
+cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l, const CUtensorMap& amap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)l.ctas, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemLayout<1, NS_F8>::BYTES;
+  cfg.dynamicSmemBytes = SmemLayout<1, NS_F8, 8 * NT8>::BYTES;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -24,14 +24,14 @@ cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.S > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<1, F16Op, NT8, false, NS_F8>, p);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<1, F16Op, NT8, false, NS_F8>, p, amap);
 }
 
 template <int NT8>
 cudaError_t set_attr() {
   cudaError_t e = cudaFuncSetAttribute(verify_kernel<1, F16Op, NT8, false, NS_F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SmemLayout<1, NS_F8>::BYTES);
+                                       SmemLayout<1, NS_F8, 8 * NT8>::BYTES);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(verify_kernel<1, F16Op, NT8, false, NS_F8>,
                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -44,13 +44,13 @@ cudaError_t prepare_fp8_attributes() {
   return set_attr<2>();
 }
 
-size_t fp8_smem_bytes() { return SmemLayout<1, NS_F8>::BYTES; }
+size_t fp8_smem_bytes() { return SmemLayout<1, NS_F8, 16>::BYTES; }
 
 int fp8_max_active_clusters(int S) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)S, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemLayout<1, NS_F8>::BYTES;
+  cfg.dynamicSmemBytes = SmemLayout<1, NS_F8, 16>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)S;
@@ -67,8 +67,9 @@ int fp8_max_active_clusters(int S) {
 }
 int fp8_pipeline_depth() { return NS_F8; }
 
-cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l) {
-  return p.M > 8 ? launch_one<2>(p, l) : launch_one<1>(p, l);
+cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l, const void* act_map) {
+  const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(act_map);
+  return p.M > 8 ? launch_one<2>(p, l, m) : launch_one<1>(p, l, m);
 }
 
 }  // namespace qmm

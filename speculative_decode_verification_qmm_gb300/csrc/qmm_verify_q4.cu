@@ -8,11 +8,11 @@ namespace {
 constexpr int NS_Q4 = 4;
 
 template <typename Op, int NT8, bool SIMT>
-cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l) {
+cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l, const CUtensorMap& amap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)l.ctas, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4>::BYTES;
+  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4, 8 * NT8>::BYTES;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -24,14 +24,14 @@ cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.S > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<0, Op, NT8, SIMT, NS_Q4>, p);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<0, Op, NT8, SIMT, NS_Q4>, p, amap);
 }
 
 template <typename Op, int NT8, bool SIMT>
 cudaError_t set_attr() {
   cudaError_t e = cudaFuncSetAttribute(verify_kernel<0, Op, NT8, SIMT, NS_Q4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SmemLayout<0, NS_Q4>::BYTES);
+                                       SmemLayout<0, NS_Q4, 8 * NT8>::BYTES);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(verify_kernel<0, Op, NT8, SIMT, NS_Q4>,
                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -50,13 +50,13 @@ cudaError_t prepare_q4_attributes() {
   return set_attr<F16Op, 2, true>();
 }
 
-size_t q4_smem_bytes() { return SmemLayout<0, NS_Q4>::BYTES; }
+size_t q4_smem_bytes() { return SmemLayout<0, NS_Q4, 16>::BYTES; }
 
 int q4_max_active_clusters(int S) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)S, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4>::BYTES;
+  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4, 16>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)S;
@@ -73,14 +73,15 @@ int q4_max_active_clusters(int S) {
 }
 int q4_pipeline_depth() { return NS_Q4; }
 
-cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l) {
+cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l, const void* act_map) {
+  const CUtensorMap& m = *reinterpret_cast<const CUtensorMap*>(act_map);
   const bool nt2 = p.M > 8;
   if (l.simt) {
-    if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, true>(p, l) : launch_one<F16Op, 1, true>(p, l);
-    return nt2 ? launch_one<Bf16Op, 2, true>(p, l) : launch_one<Bf16Op, 1, true>(p, l);
+    if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, true>(p, l, m) : launch_one<F16Op, 1, true>(p, l, m);
+    return nt2 ? launch_one<Bf16Op, 2, true>(p, l, m) : launch_one<Bf16Op, 1, true>(p, l, m);
   }
-  if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, false>(p, l) : launch_one<F16Op, 1, false>(p, l);
-  return nt2 ? launch_one<Bf16Op, 2, false>(p, l) : launch_one<Bf16Op, 1, false>(p, l);
+  if (l.f16_ops) return nt2 ? launch_one<F16Op, 2, false>(p, l, m) : launch_one<F16Op, 1, false>(p, l, m);
+  return nt2 ? launch_one<Bf16Op, 2, false>(p, l, m) : launch_one<Bf16Op, 1, false>(p, l, m);
 }
 
 }  // namespace qmm

@@ -138,15 +138,6 @@ __host__ __device__ constexpr uint32_t tc_idesc(uint32_t ab) {
   return (1u << 4) | (ab << 7) | (ab << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
 // 8 nibbles (element 2p in nibble p, 2p + 1 in nibble p + 4) -> 4 registers of
 // (q - 8) pairs in element order.
 template <typename Op>

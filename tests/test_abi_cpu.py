@@ -119,6 +119,13 @@ def test_host_validation_without_device(L):
     assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_SHAPE  # N % 128
     d.flags = q.QMM_FLAG_SIMT
     assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_TCGEN05  # tcgen05 serves bf16 Q4_0 only
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.format = q.QMM_FMT_Q4_0
+    d.flags = q.QMM_FLAG_TCGEN05 | q.QMM_FLAG_HADAMARD32
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_TCGEN05 | q.QMM_FLAG_SIMT
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
     assert h.value is None
     # tool entry points validate shapes first
     assert L.qmm_quantize_q4_0(None, 4, 32, 0, None, None) == q.QMM_ERR_INVALID_ARG

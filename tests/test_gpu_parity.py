@@ -122,27 +122,33 @@ def test_quantize_fp8_bit_exact(hadamard):
 
 
 # ---------------------------------------------------------------- verify product
+KERNELS = {"mma": {}, "tc": {"tcgen05": True}, "simt": {"simt": True}}
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tc", "simt"])
 @pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 15, 16])
-def test_verify_q4_small_config(M):
+def test_verify_q4_small_config(M, kernel):
     # M rows, K = 512, N = 256 (the single-shape parity workload), seed 0
     w, a, spec = synth.workload("q4_small", M=M)
     N, K = spec["N"], spec["K"]
     blocks = O.q4_0_quantize(w)
-    mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K)
-    check_verify(mat, O.FMT_Q4_0, blocks, None, N, K, a, False, what=f"q4 M={M}")
+    mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K, **KERNELS[kernel])
+    check_verify(mat, O.FMT_Q4_0, blocks, None, N, K, a, False, what=f"q4 {kernel} M={M}")
 
 
-@pytest.mark.parametrize("N,K,splits,hadamard,simt", [
-    (424, 1376, 0, False, False), (424, 1376, 3, False, False), (424, 1376, 6, True, False),
-    (1000, 2560, 0, True, False), (256, 512, 2, False, True), (424, 1376, 3, True, True),
-    (8, 32, 0, False, False), (1, 64, 0, False, False), (129, 4096, 16, False, False),
+@pytest.mark.parametrize("N,K,splits,hadamard,kernel", [
+    (424, 1376, 0, False, "mma"), (424, 1376, 3, False, "mma"), (424, 1376, 6, True, "mma"),
+    (1000, 2560, 0, True, "mma"), (256, 512, 2, False, "simt"), (424, 1376, 3, True, "simt"),
+    (8, 32, 0, False, "mma"), (1, 64, 0, False, "mma"), (129, 4096, 16, False, "mma"),
+    (424, 1376, 0, False, "tc"), (424, 1376, 3, False, "tc"), (8, 32, 0, False, "tc"),
+    (129, 4096, 16, False, "tc"), (1000, 2560, 5, False, "tc"),
 ])
 @pytest.mark.parametrize("M", [1, 16])
-def test_verify_q4_ragged(N, K, splits, hadamard, simt, M):
-    mat, blocks = q4_matrix(N, K, 40 + N + K, hadamard=hadamard, simt=simt, k_splits=splits)
+def test_verify_q4_ragged(N, K, splits, hadamard, kernel, M):
+    mat, blocks = q4_matrix(N, K, 40 + N + K, hadamard=hadamard, k_splits=splits, **KERNELS[kernel])
     a = synth.activations(M, K, 41 + K, outliers=True)
     check_verify(mat, O.FMT_Q4_0, blocks, None, N, K, a, hadamard,
-                 what=f"q4 N={N} K={K} S={splits} H={hadamard} simt={simt} M={M}")
+                 what=f"q4 N={N} K={K} S={splits} H={hadamard} {kernel} M={M}")
 
 
 @pytest.mark.parametrize("N,K,splits,hadamard", [(384, 896, 0, False), (384, 896, 3, False),
@@ -154,11 +160,12 @@ def test_verify_fp8(N, K, splits, hadamard, M):
     check_verify(mat, O.FMT_FP8, codes, scales, N, K, a, hadamard, what=f"fp8 N={N} K={K} M={M}")
 
 
-@pytest.mark.parametrize("fmt,hadamard", [("q4", False), ("q4", True), ("fp8", False)])
+@pytest.mark.parametrize("fmt,hadamard", [("q4", False), ("q4", True), ("q4tc", False),
+                                          ("fp8", False)])
 def test_rows_bit_identical_for_every_M(fmt, hadamard):
     N, K = 640, 2048
-    if fmt == "q4":
-        mat, _ = q4_matrix(N, K, 90, hadamard=hadamard, k_splits=4)
+    if fmt.startswith("q4"):
+        mat, _ = q4_matrix(N, K, 90, hadamard=hadamard, k_splits=4, tcgen05=(fmt == "q4tc"))
     else:
         mat, _, _ = fp8_matrix(N, K, 90, k_splits=4)
     a = synth.activations(16, K, 91, outliers=True)
@@ -202,6 +209,7 @@ def test_leading_dimensions_and_untouched_memory():
 # ---------------------------------------------------------------- full-size shapes
 FULL = [
     ("q4_attn", (1, 8, 16), False),
+    ("q4_attn_tc", (1, 16), False),
     ("q4_gateup", (16,), False),
     ("q4_down", (16,), False),
     ("q4_gateup", (16,), True),
@@ -215,7 +223,8 @@ def test_full_size_sampled_rows(name, Ms, hadamard):
     """The workloads at full size, in the launch configuration the benchmark
     uses (planner's choice), compared on sampled rows: every row tile boundary,
     both ends, and random rows."""
-    spec = synth.SHAPES[name]
+    tc = name.endswith("_tc")
+    spec = synth.SHAPES[name[:-3] if tc else name]
     N, K, b = spec["N"], spec["K"], spec["seed"]
     w = synth.weights(N, K, b)
     rng = np.random.default_rng(b)
@@ -225,7 +234,8 @@ def test_full_size_sampled_rows(name, Ms, hadamard):
     if spec["fmt"] == "q4_0":
         blocks = O.q4_0_quantize_h32(w) if hadamard else O.q4_0_quantize(w)
         del w
-        mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K, hadamard=hadamard)
+        mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K, hadamard=hadamard,
+                       tcgen05=tc)
         fmt, wb, sc = O.FMT_Q4_0, blocks, None
     else:
         codes, scales = O.fp8_quantize(w)
@@ -286,12 +296,13 @@ def test_injected_allocation_failure_leaks_nothing():
     mat.close()
 
 
-def test_bounded_wait_timeout_path_and_recovery():
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_bounded_wait_timeout_path_and_recovery(kernel):
     """A wait limit of 0 makes every bounded device wait give up at once; the
     kernel records the timeout, drains its own copies and returns.  Nothing
     hangs; the handle works again after qmm_sync_status."""
     N, K, M = 512, 4096, 8
-    mat, blocks = q4_matrix(N, K, 160, k_splits=2)
+    mat, blocks = q4_matrix(N, K, 160, k_splits=2, **KERNELS[kernel])
     a = synth.activations(M, K, 161, outliers=True)
     act = bf16_cuda(a)
     q.qmm_debug_set_wait_limit(mat.handle, 0)
