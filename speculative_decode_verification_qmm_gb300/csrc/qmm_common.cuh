@@ -49,7 +49,9 @@ namespace qmm {
 constexpr int TILE_N = 128;           // rows of W per CTA tile
 constexpr int STAGE_CHUNKS = 4;       // column chunks per stage in the layout
 constexpr int COMPUTE_WARPS = 8;      // warps that compute: chunk x half of the tile's rows
-constexpr int THREADS = (COMPUTE_WARPS + 1) * 32;  // + one producer warp
+// No separate producer warp: the compute warps also issue the copies, so two
+// CTAs (16 warps) keep exactly four warps per SM sub-partition.
+constexpr int THREADS = COMPUTE_WARPS * 32;
 constexpr int MAX_M = 16;
 
 // Q4_0

@@ -1,12 +1,14 @@
 // qmm_verify.cuh -- the weight-streaming verify kernel.
 //
-// One CTA = one row tile of W (128 rows) x one K split.  A producer thread
-// streams the CTA's stages through an NS-deep shared-memory ring.  A stage is
-// four column chunks and each chunk has its own full/empty mbarrier pair: one
-// bulk copy of the chunk's repacked weights and one tensor-map box of the
-// activations (R = 8 or 16 drafted rows x the chunk's columns) complete its
-// full barrier.  Eight compute warps (chunk x half of the tile's rows) wait for
-// their own chunk only, dequantize their codes in registers straight into
+// One CTA = one row tile of W (128 rows) x one K split; it streams its stages
+// through an NS-deep shared-memory ring.  A stage is four column chunks and
+// each chunk has its own full mbarrier: one bulk copy of the chunk's repacked
+// weights and one tensor-map box of the activations (R = 8 or 16 drafted rows
+// x the chunk's columns) complete it.  There is no producer warp: thread 0
+// requests the first NS stages, and afterwards the last warp to finish with a
+// chunk (a shared-memory counter picks it, nobody waits) requests the same
+// chunk of the stage NS ahead into the slot it just freed.  Eight compute
+// warps (chunk x half of the tile's rows) wait for their own chunk only, dequantize their codes in registers straight into
 // mma.sync A fragments (weights are the MMA's M dimension, drafted rows its
 // N = 8 or 16 dimension, "swap AB"), keep fp32 accumulators in registers
 // across the CTA's K range, and apply the per-block (Q4_0) or per-tile (FP8)
@@ -67,7 +69,8 @@ struct SmemLayout {
   static constexpr int A_CHUNK = F::CHUNK_K * R * 2;  // one tensor-map box: R rows x CHUNK_K
   static constexpr int A_STAGE = STAGE_CHUNKS * A_CHUNK;
   static constexpr int A_BYTES = NS * A_STAGE;
-  static constexpr int BAR_OFF = A_OFF + A_BYTES;  // full[NS][4], then empty[NS][4]
+  // full[NS][4] mbarriers, then per (slot, chunk) {finished-warp count, last stage requested}
+  static constexpr int BAR_OFF = A_OFF + A_BYTES;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NS * STAGE_CHUNKS * 8;
   static constexpr int BYTES = FLAG_OFF + 16 + 1024;
   // epilogue areas (reuse the weight ring): chunk partials [chunk][row][RED_PITCH],
@@ -279,8 +282,7 @@ __device__ __forceinline__ void q4_chunk_simt(uint32_t unit, uint32_t achunk, in
 // qmm_common.cuh) whose boxes are CHUNK_K columns x R rows, swizzled by
 // 2 x CHUNK_K bytes.
 // ---------------------------------------------------------------------------
-// Two CTAs per SM: 18 warps need at most 5 warps' registers per SM
-// sub-partition, i.e. 96 registers per thread.
+// Two CTAs per SM: 16 warps, four per SM sub-partition, up to 128 registers.
 template <int FMT, typename Op, int NT8, bool SIMT, int NS>
 __global__ void __launch_bounds__(THREADS, 2)
     verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap amap) {
@@ -301,21 +303,22 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t s_w = s_base + L::W_OFF;
   const uint32_t s_a = s_base + L::A_OFF;
   const uint32_t s_full = s_base + L::BAR_OFF;        // [slot][chunk]
-  const uint32_t s_empty = s_full + NS * NCH * 8;     // [slot][chunk]
   auto full_bar = [&](int slot, int c) { return s_full + (uint32_t)(slot * NCH + c) * 8u; };
-  auto empty_bar = [&](int slot, int c) { return s_empty + (uint32_t)(slot * NCH + c) * 8u; };
-  // [0] abort, [2] chunk copies issued by the producer
+  // [slot][chunk][0]: warps done with the chunk's current stage; [1]: last stage requested
+  int* s_chunk = reinterpret_cast<int*>(smem + L::BAR_OFF + NS * NCH * 8);
+  // MMA warps: two per chunk; CUDA-core warps: every warp reads every chunk
+  constexpr int READERS = SIMT ? COMPUTE_WARPS : COMPUTE_WARPS / NCH;
+  // [0] abort
   volatile int* s_flag = reinterpret_cast<volatile int*>(smem + L::FLAG_OFF);
 
   if (tid == 0) {
     for (int i = 0; i < NS * NCH; ++i) {
       mbar_init(s_full + 8 * i, 1);
-      // MMA warps: two per chunk; CUDA-core warps: every warp reads every chunk
-      mbar_init(s_empty + 8 * i, SIMT ? COMPUTE_WARPS : COMPUTE_WARPS / NCH);
+      s_chunk[2 * i] = 0;
+      s_chunk[2 * i + 1] = -1;
     }
     s_flag[0] = 0;
     s_flag[1] = 0;
-    s_flag[2] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -328,50 +331,50 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int k0 = (int)(gstage0 * F::STAGE_K);  // first column of this CTA (a multiple of 8)
   constexpr uint32_t CHUNK_TX = F::CHUNK_BYTES + L::A_CHUNK;
 
-  if (warp == COMPUTE_WARPS) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const int pre = nst < NS ? nst : NS;
-      // Weights never depend on earlier kernels: fetch the first stages now.
-      for (int i = 0; i < pre; ++i)
-        for (int c = 0; c < NCH; ++c) {
-          mbar_arrive_expect_tx(full_bar(i, c), CHUNK_TX);
-          bulk_g2s_hint(s_w + i * F::STAGE_BYTES + c * F::CHUNK_BYTES,
-                        wsrc + (size_t)i * F::STAGE_BYTES + c * F::CHUNK_BYTES, F::CHUNK_BYTES,
-                        full_bar(i, c), pol);
-        }
-      // Activations may be written by the previous kernel: wait for it.
-      pdl_wait();
-      for (int i = 0; i < pre; ++i)
-        for (int c = 0; c < NCH; ++c)
-          tma_load_2d(s_a + i * L::A_STAGE + c * L::A_CHUNK, &amap,
-                      k0 + i * F::STAGE_K + c * F::CHUNK_K, 0, full_bar(i, c));
-      int issued = pre * NCH;
-      bool ok = true;
-      for (int i = NS; i < nst && ok; ++i) {
-        const int slot = i % NS;
-        for (int c = 0; c < NCH; ++c) {
-          if (!mbar_wait_bounded(empty_bar(slot, c), ((i / NS) - 1) & 1, p.wait_limit_ns)) {
-            atomicOr(p.status, DEV_ERR_TIMEOUT_EMPTY);
-            s_flag[0] = 1;
-          }
-          if (s_flag[0]) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(slot, c), CHUNK_TX);
-          bulk_g2s_hint(s_w + slot * F::STAGE_BYTES + c * F::CHUNK_BYTES,
-                        wsrc + (size_t)i * F::STAGE_BYTES + c * F::CHUNK_BYTES, F::CHUNK_BYTES,
-                        full_bar(slot, c), pol);
-          tma_load_2d(s_a + slot * L::A_STAGE + c * L::A_CHUNK, &amap,
-                      k0 + i * F::STAGE_K + c * F::CHUNK_K, 0, full_bar(slot, c));
-          ++issued;
-        }
-      }
-      s_flag[2] = issued;
+  const uint64_t pol = policy_evict_first();
+  // Request chunk c of stage i into ring slot i % NS (weights, then activations).
+  auto request = [&](int i, int c, bool weights, bool act) {
+    const int slot = i % NS;
+    if (weights) {
+      mbar_arrive_expect_tx(full_bar(slot, c), CHUNK_TX);
+      bulk_g2s_hint(s_w + slot * F::STAGE_BYTES + c * F::CHUNK_BYTES,
+                    wsrc + (size_t)i * F::STAGE_BYTES + c * F::CHUNK_BYTES, F::CHUNK_BYTES,
+                    full_bar(slot, c), pol);
+      s_chunk[2 * (slot * NCH + c) + 1] = i;
     }
+    if (act)
+      tma_load_2d(s_a + slot * L::A_STAGE + c * L::A_CHUNK, &amap,
+                  k0 + i * F::STAGE_K + c * F::CHUNK_K, 0, full_bar(slot, c));
+  };
+  // The last of the READERS warps done with chunk c of stage i (ring slot
+  // i % NS) requests the same chunk of stage i + NS into that slot.  Called
+  // by lane 0 after the warp's reads of the chunk.
+  auto release = [&](int i, int c) {
+    const int slot = i % NS;
+    int* cnt = s_chunk + 2 * (slot * NCH + c);
+    __threadfence_block();
+    const int done = atomicAdd(cnt, 1) + 1;
+    __threadfence_block();
+    if (done == READERS) {
+      *cnt = 0;
+      if (i + NS < nst && !s_flag[0]) {
+        fence_proxy_async_smem();  // the readers' loads come before the copy's writes
+        request(i + NS, c, true, true);
+      }
+    }
+  };
+
+  if (tid == 0) {
+    const int pre = nst < NS ? nst : NS;
+    // Weights never depend on earlier kernels: fetch the first stages now.
+    for (int i = 0; i < pre; ++i)
+      for (int c = 0; c < NCH; ++c) request(i, c, true, false);
+    // Activations may be written by the previous kernel: wait for it.
+    pdl_wait();
+    for (int i = 0; i < pre; ++i)
+      for (int c = 0; c < NCH; ++c) request(i, c, false, true);
   }
+  __syncwarp();
 
   // Accumulators (registers) of the compute warps.
   float acc[WARP_SUBTILES][2][4];
@@ -413,7 +416,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         else
           f8_stage_mma<NT8>(wch, ach, fs, lane, acc);
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(slot, chunk));
+        if (lane == 0) release(i, chunk);
+        __syncwarp();
         if (s_flag[0]) break;
       }
     } else {
@@ -434,7 +438,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                                     warp * F::UNIT_BYTES,
                                 s_a + slot * L::A_STAGE + c * L::A_CHUNK, lane, M, accs);
           __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(slot, c));
+          if (lane == 0) release(i, c);
+          __syncwarp();
         }
         if (s_flag[0]) ok = false;
       }
@@ -443,16 +448,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   const bool aborted = s_flag[0] != 0;
   if (aborted) {
-    // Give up: no copy issued by this CTA may still be landing in shared memory
-    // when the CTA exits.  Only the chunks of the last NS issued stages can be
-    // in flight, and each of them is the latest phase armed on its barrier;
-    // that phase completes when its bytes land, whether or not a compute warp
-    // waited for it.
-    if (warp == COMPUTE_WARPS && lane == 0) {
-      const int issued = s_flag[2];
-      for (int x = issued - NS * NCH < 0 ? 0 : issued - NS * NCH; x < issued; ++x) {
-        const int i = x / NCH, c = x % NCH;
-        if (!mbar_wait_bounded(full_bar(i % NS, c), (i / NS) & 1, 1000000000ull))
+    // Give up: no copy requested by this CTA may still be landing in shared
+    // memory when the CTA exits.  The last stage requested into each (slot,
+    // chunk) is the latest phase armed on its barrier; that phase completes
+    // when its bytes land, whether or not a compute warp waited for it.
+    if (tid == 0) {
+      for (int x = 0; x < NS * NCH; ++x) {
+        const int i = s_chunk[2 * x + 1];
+        if (i >= 0 && !mbar_wait_bounded(s_full + 8u * x, (i / NS) & 1, 1000000000ull))
           atomicOr(p.status, DEV_ERR_TIMEOUT_DRAIN);
       }
     }
