@@ -20,11 +20,19 @@ namespace {
 constexpr uint64_t HANDLE_MAGIC = 0x514D4D5645524946ull;  // "QMMVERIF"
 constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
-// Planner constants: HBM copy bandwidth of the part and what one CTA with its
-// pipeline full sustains (both only rank candidate plans; see plan()).
+// Planner constants (they only rank candidate plans; see make_plan()): HBM
+// copy bandwidth of the part; tcgen05 kernel: what one CTA with its pipeline
+// full sustains and the cluster reduction; mma.sync kernels: one stage's time
+// for a CTA alone on its SM and for each of two CTAs sharing one (measured at
+// M <= 8), the fixed cost of a call (first bytes, epilogue) and of the split-K
+// fix-up by the last split to arrive.
 constexpr double PLAN_HBM_BPS = 6.8e12;
 constexpr double PLAN_CTA_BPS = 30e9;
 constexpr double PLAN_CLUSTER_REDUCE_S = 0.4e-6;
+constexpr double PLAN_STAGE_1_S = 0.35e-6;
+constexpr double PLAN_STAGE_2_S = 0.50e-6;
+constexpr double PLAN_FIXED_S = 1.5e-6;
+constexpr double PLAN_FIXUP_S = 0.8e-6;
 
 struct Plan {
   int n_tiles = 0, S = 1, spc = 1, stage_k = 0, stage_bytes = 0, depth = 0;
@@ -49,6 +57,8 @@ struct qmm_handle {
   int64_t act_ld = 0;
   size_t act_bytes = 0;
   float* out_scale = nullptr;  // [MAX_M][S]
+  float* ws = nullptr;         // mma.sync kernels, S > 1: split partials
+  int* counters = nullptr;     // mma.sync kernels, S > 1: [n_tiles] arrivals
   int* status = nullptr;       // device error word
   uint16_t* stage_act = nullptr;  // host-buffer path: [MAX_M][act_pitch]
   int64_t stage_act_pitch = 0;
@@ -108,10 +118,12 @@ int cuda_fail(qmm_handle* h, cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Choose the K split count S (= cluster size).  Candidates keep every CTA
-// resident in one wave (two CTAs per SM; for S > 1 as many clusters as the
-// device holds at once); each is scored by the time to stream its padded bytes
-// at min(HBM bandwidth, CTAs x per-CTA rate) plus the cluster reduction.
+// Choose the K split count S.  With S > 1 every CTA stays resident in one
+// wave (two CTAs per SM; tcgen05: as many clusters of S as the device holds at
+// once).  tcgen05: score = time to stream the padded bytes at min(HBM
+// bandwidth, CTAs x per-CTA rate) plus the cluster reduction.  mma.sync:
+// score = max(stream time of the padded bytes, stages per CTA x stage time)
+// plus the fixed cost and the fix-up; near-ties go to the plan with more CTAs.
 Plan make_plan(int fmt, bool tc, int64_t N, int64_t K, int sm_count, int forced_splits) {
   Plan p;
   p.tc = tc;
@@ -133,24 +145,33 @@ Plan make_plan(int fmt, bool tc, int64_t N, int64_t K, int sm_count, int forced_
   const int64_t max_ctas = 2ll * sm_count;
   double best = 1e30;
   int best_s = 1;
+  int64_t best_ctas = 0;
   for (int S = 1; S <= MAX_SPLITS && S <= p.nst; ++S) {
     const int64_t spc = ceil_div(p.nst, S);
     if (ceil_div(p.nst, spc) != S) continue;
     const int64_t ctas = (int64_t)p.n_tiles * S;
-    if (S > 1) {
-      if (ctas > max_ctas) break;
-      const int clusters = tc ? tc_max_active_clusters(S)
-                              : (fmt == 0 ? q4_max_active_clusters(S) : fp8_max_active_clusters(S));
-      if (clusters > 0 && p.n_tiles > clusters) continue;
-    }
+    if (S > 1 && ctas > max_ctas) break;
     const double bytes = (double)ctas * spc * p.stage_bytes;
-    double rate = (double)ctas * PLAN_CTA_BPS;
-    if (rate > PLAN_HBM_BPS) rate = PLAN_HBM_BPS;
-    double t = bytes / rate;
-    if (S > 1) t += PLAN_CLUSTER_REDUCE_S;
-    if (t < best * 0.999) {
-      best = t;
+    double t;
+    if (tc) {
+      if (S > 1) {
+        const int clusters = tc_max_active_clusters(S);
+        if (clusters > 0 && p.n_tiles > clusters) continue;
+      }
+      double rate = (double)ctas * PLAN_CTA_BPS;
+      if (rate > PLAN_HBM_BPS) rate = PLAN_HBM_BPS;
+      t = bytes / rate + (S > 1 ? PLAN_CLUSTER_REDUCE_S : 0.0);
+    } else {
+      const int64_t waves = ceil_div(ctas, max_ctas);
+      const double stage = ctas > sm_count ? PLAN_STAGE_2_S : PLAN_STAGE_1_S;
+      const double compute = (double)waves * spc * stage;
+      const double stream = bytes / PLAN_HBM_BPS;
+      t = (compute > stream ? compute : stream) + PLAN_FIXED_S + (S > 1 ? PLAN_FIXUP_S : 0.0);
+    }
+    if (t < best * 0.99 || (t <= best * 1.01 && ctas > best_ctas)) {
+      if (t < best) best = t;
       best_s = S;
+      best_ctas = ctas;
     }
   }
   fix(best_s);
@@ -166,6 +187,8 @@ void free_handle(qmm_handle* h) {
   cudaFree(h->f8_scale);
   cudaFree(h->act_scratch);
   cudaFree(h->out_scale);
+  cudaFree(h->ws);
+  cudaFree(h->counters);
   cudaFree(h->status);
   cudaFree(h->stage_act);
   cudaFree(h->stage_out);
@@ -368,6 +391,10 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   if (fmt == 1) QMM_ALLOC(h->f8_scale, (size_t)p.n_tiles * stages_total * sizeof(float));
   QMM_ALLOC(h->act_scratch, h->act_bytes);
   QMM_ALLOC(h->out_scale, (size_t)MAX_M * p.S * sizeof(float));
+  if (!p.tc && p.S > 1) {
+    QMM_ALLOC(h->ws, (size_t)p.n_tiles * p.S * MAX_M * TILE_N * sizeof(float));
+    QMM_ALLOC(h->counters, (size_t)p.n_tiles * sizeof(int));
+  }
   QMM_ALLOC(h->status, sizeof(int));
   QMM_ALLOC(h->stage_act, (size_t)MAX_M * h->stage_act_pitch * sizeof(uint16_t));
   QMM_ALLOC(h->stage_out, (size_t)MAX_M * d->N * sizeof(float));
@@ -395,6 +422,9 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   if (e != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->act_scratch, 0, h->act_bytes, st)) != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
+  if (h->counters &&
+      (e = cudaMemsetAsync(h->counters, 0, (size_t)p.n_tiles * sizeof(int), st)) != cudaSuccess)
+    goto fail;
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) goto fail;
   cudaFree(tmp_w);
   cudaFree(tmp_s);
@@ -468,6 +498,8 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   vp.M = M;
   vp.S = p.S;
   vp.spc = p.spc;
+  vp.ws = h->ws;
+  vp.counters = h->counters;
   vp.wait_limit_ns = h->wait_limit_ns;
   VerifyLaunch vl;
   vl.fmt = h->fmt;
@@ -539,7 +571,8 @@ int qmm_get_info(qmm_t h, qmm_info* info) {
   info->weight_bytes = h->fmt == 0 ? h->N * h->K / 32 * 18
                                    : h->N * h->K + 4 * (h->N / 128) * (h->K / 128);
   info->device_weight_bytes = (int64_t)h->wdev_bytes;
-  info->scratch_bytes = (int64_t)(h->act_bytes + MAX_M * p.S * sizeof(float) + sizeof(int));
+  info->scratch_bytes = (int64_t)(h->act_bytes + MAX_M * p.S * sizeof(float) + sizeof(int)) +
+                        (h->ws ? (int64_t)p.n_tiles * p.S * MAX_M * TILE_N * 4 + (int64_t)p.n_tiles * 4 : 0);
   info->n_tiles = p.n_tiles;
   info->k_splits = p.S;
   info->ctas = p.n_tiles * p.S;
@@ -700,6 +733,8 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   vp.M = M;
   vp.S = p.S;
   vp.spc = p.spc;
+  vp.ws = h->ws;
+  vp.counters = h->counters;
   vp.wait_limit_ns = h->wait_limit_ns;
   VerifyLaunch vl;
   vl.fmt = h->fmt;

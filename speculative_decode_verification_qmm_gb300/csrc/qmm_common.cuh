@@ -80,8 +80,10 @@ struct VerifyParams {
   int64_t ldo;
   int64_t N;
   int M;
-  int S;                     // K splits = CTAs per cluster
+  int S;                     // K splits per row tile (tcgen05 kernel: CTAs per cluster)
   int spc;                   // stages per CTA
+  float* ws;                 // mma.sync kernels, S > 1: [n_tiles][S][MAX_M][TILE_N] partials
+  int* counters;             // mma.sync kernels, S > 1: [n_tiles] arrivals, zero between calls
   uint64_t wait_limit_ns;    // bounded waits give up after this (0: at once)
 };
 

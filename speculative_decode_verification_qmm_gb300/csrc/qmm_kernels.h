@@ -25,10 +25,7 @@ size_t q4_smem_bytes();
 size_t fp8_smem_bytes();
 cudaError_t prepare_q4_attributes();
 cudaError_t prepare_fp8_attributes();
-// Clusters of S CTAs the device can hold at once (-1 if the query fails).
-int q4_max_active_clusters(int S);
-int fp8_max_active_clusters(int S);
-constexpr int MAX_SPLITS = 16;  // K splits = cluster size (16 needs the non-portable opt-in)
+constexpr int MAX_SPLITS = 16;  // K splits per row tile (tcgen05: = cluster size, 16 is non-portable)
 
 // tcgen05 kernel (Q4_0): its weight layout, repack, dequantization and launch.
 // act_map points to a CUtensorMap over the activation rows (3-D view

@@ -15,10 +15,10 @@
 // scale with packed fp32 FMAs.  The epilogue adds the four chunk partials in a
 // fixed order through shared memory, multiplies by the pre-pass's per-(row,
 // split) power-of-two factor, and either writes `out` (one split) or, when the
-// K range is split, leaves its partial in shared memory: the S CTAs of a row
-// tile form one thread-block cluster and each adds a slice of the tile's rows
-// over the S partials through distributed shared memory, in split order
-// (deterministic, no global scratch, no atomics).
+// K range is split, writes its partial to the handle's workspace and bumps the
+// tile's arrival count: the last of the S splits to arrive adds the S partials
+// in split order and writes the tile (deterministic; no split waits for
+// another, so they need not be resident at the same time).
 //
 // The summation order of every output element is fixed by (N, K, plan) and
 // never depends on M, so row m of the result is bit-identical for M = 1..16.
@@ -74,13 +74,10 @@ struct SmemLayout {
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NS * STAGE_CHUNKS * 8;
   static constexpr int BYTES = FLAG_OFF + 16 + 1024;
   // epilogue areas (reuse the weight ring): chunk partials [chunk][row][RED_PITCH],
-  // then the CTA partial read by the cluster [row][CP_PITCH]
+  // (the split partials go to the workspace in global memory)
   static constexpr int RED_PITCH = MAX_M + 2;  // floats per row
   static constexpr int RED_BYTES = STAGE_CHUNKS * TILE_N * RED_PITCH * 4;
-  static constexpr int CP_PITCH = MAX_M + 1;
-  static constexpr int CP_OFF = RED_BYTES;
-  static constexpr int CP_BYTES = TILE_N * CP_PITCH * 4;
-  static_assert(CP_OFF + CP_BYTES <= NS * F::STAGE_BYTES, "epilogue areas must fit in the ring");
+  static_assert(RED_BYTES <= NS * F::STAGE_BYTES, "the epilogue area must fit in the ring");
   static_assert(A_OFF % 1024 == 0 && A_CHUNK % (F::CHUNK_K * 2 * 8) == 0,
                 "every box starts on a swizzle period");
   static_assert(F::CHUNK_BYTES % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
@@ -460,16 +457,14 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
     }
     __syncthreads();
-    // An aborted CTA writes nothing but still takes part in the cluster
-    // barriers below, so that no CTA of its cluster can wait for it forever.
+    // An aborted CTA writes nothing but still counts its arrival, so that the
+    // tile's count returns to zero for the next call.
   }
 
   // ------------------------------------------------------------ epilogue
   pdl_wait();  // order our writes after every earlier kernel's
   float* red = reinterpret_cast<float*>(smem + L::W_OFF);
-  float* cpart = reinterpret_cast<float*>(smem + L::W_OFF + L::CP_OFF);
   constexpr int RP = L::RED_PITCH;
-  constexpr int CP = L::CP_PITCH;
   if (warp < COMPUTE_WARPS && !aborted) {
     const int g = lane >> 2, t = lane & 3;
     if constexpr (!SIMT) {
@@ -507,7 +502,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
 
   // The CTA's partial: the chunk partials added in chunk order, times the
-  // pre-pass's factor of this (row, split).
+  // pre-pass's factor of this (row, split).  With one split it is the result;
+  // otherwise it goes to the handle's workspace, [tile][split][m][row].
+  float* mine = p.ws + ((int64_t)tile * p.S + split) * (MAX_M * TILE_N);
   if (tid < TILE_N && !aborted) {
     constexpr int NRED = SIMT ? 1 : STAGE_CHUNKS;
     const int64_t n = (int64_t)tile * TILE_N + tid;
@@ -519,36 +516,47 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (p.S == 1) {
         if (n < p.N) p.out[(int64_t)m * p.ldo + n] = v;
       } else {
-        cpart[tid * CP + m] = v;
+        mine[m * TILE_N + tid] = v;
       }
     }
   }
   if (p.S == 1) return;
 
-  // Split K: the S CTAs of this row tile are one cluster.  CTA `split` adds
-  // the S partials of its slice of the tile's rows, in split order.
-  cluster_sync_all();
-  if (!aborted) {
-    const int r0 = (split * TILE_N) / p.S, r1 = ((split + 1) * TILE_N) / p.S;
-    const int nr = r1 - r0;
-    const uint32_t cbase = smem_u32(cpart);
-    for (int idx = tid; idx < nr * M; idx += THREADS) {
-      const int m = idx / nr, row = r0 + idx % nr;
-      const uint32_t la = cbase + (uint32_t)(row * CP + m) * 4u;
-      float x[16];
+  // Split K: the last of the tile's S CTAs to arrive adds the S partials in
+  // split order (the count goes back to zero for the next call).  Nobody
+  // waits for anybody, so the splits need not be resident together.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(p.counters + tile, 1);
+    const bool last = prev == p.S - 1;
+    if (last) p.counters[tile] = 0;
+    s_flag[1] = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_flag[1] && !aborted) {
+    __threadfence();
+    const float* base = p.ws + (int64_t)tile * p.S * (MAX_M * TILE_N);
+    // float4 piece q: drafted row q / 32, rows 4 (q % 32) .. + 3
+    for (int q = tid; q < M * (TILE_N / 4); q += THREADS) {
+      const int m = q / (TILE_N / 4), row = 4 * (q % (TILE_N / 4));
+      float4 v = __ldcg(reinterpret_cast<const float4*>(base + m * TILE_N + row));
+      for (int sp = 1; sp < p.S; ++sp) {
+        const float4 x =
+            __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)sp * MAX_M + m) * TILE_N + row));
+        v.x += x.x;
+        v.y += x.y;
+        v.z += x.z;
+        v.w += x.w;
+      }
+      const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s < p.S) x[s] = ld_dsmem_f32(dsmem_map(la, (uint32_t)s));
-      float v = x[0];
-#pragma unroll
-      for (int s = 1; s < 16; ++s)
-        if (s < p.S) v += x[s];
-      const int64_t n = (int64_t)tile * TILE_N + row;
-      if (n < p.N) p.out[(int64_t)m * p.ldo + n] = v;
+      for (int r = 0; r < 4; ++r) {
+        const int64_t n = (int64_t)tile * TILE_N + row + r;
+        if (n < p.N) p.out[(int64_t)m * p.ldo + n] = vals[r];
+      }
     }
   }
-  // Keep this CTA's shared memory alive until every CTA of the cluster has read it.
-  cluster_sync_all();
 }
 
 }  // namespace qmm

@@ -14,16 +14,11 @@ cudaError_t launch_one(const VerifyParams& p, const VerifyLaunch& l, const CUten
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4, 8 * NT8>::BYTES;
   cfg.stream = l.stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  // the K splits of a row tile form one cluster (they reduce through DSMEM)
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)p.S;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.S > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, verify_kernel<0, Op, NT8, SIMT, NS_Q4>, p, amap);
 }
 
@@ -32,9 +27,7 @@ cudaError_t set_attr() {
   cudaError_t e = cudaFuncSetAttribute(verify_kernel<0, Op, NT8, SIMT, NS_Q4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SmemLayout<0, NS_Q4, 8 * NT8>::BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(verify_kernel<0, Op, NT8, SIMT, NS_Q4>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 }  // namespace
 
@@ -52,25 +45,6 @@ cudaError_t prepare_q4_attributes() {
 
 size_t q4_smem_bytes() { return SmemLayout<0, NS_Q4, 16>::BYTES; }
 
-int q4_max_active_clusters(int S) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)S, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemLayout<0, NS_Q4, 16>::BYTES;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_kernel<0, Bf16Op, 2, false, NS_Q4>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return -1;
-  }
-  return n;
-}
 int q4_pipeline_depth() { return NS_Q4; }
 
 cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l, const void* act_map) {
