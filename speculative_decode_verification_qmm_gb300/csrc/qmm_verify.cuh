@@ -525,17 +525,23 @@ __global__ void __launch_bounds__(THREADS, 2)
   // Split K: the last of the tile's S CTAs to arrive adds the S partials in
   // split order (the count goes back to zero for the next call).  Nobody
   // waits for anybody, so the splits need not be resident together.
-  __threadfence();
+  // One GPU-scope acquire-release add by thread 0 after the CTA barrier:
+  // it releases every thread's partial (ordered before it by the barrier)
+  // and, for the last arrival, acquires the other splits' partials for the
+  // threads ordered after it by the second barrier.
   __syncthreads();
   if (tid == 0) {
-    const int prev = atomicAdd(p.counters + tile, 1);
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(p.counters + tile)
+                 : "memory");
     const bool last = prev == p.S - 1;
     if (last) p.counters[tile] = 0;
     s_flag[1] = last ? 1 : 0;
   }
   __syncthreads();
   if (s_flag[1] && !aborted) {
-    __threadfence();
     const float* base = p.ws + (int64_t)tile * p.S * (MAX_M * TILE_N);
     // float4 piece q: drafted row q / 32, rows 4 (q % 32) .. + 3
     for (int q = tid; q < M * (TILE_N / 4); q += THREADS) {
