@@ -349,9 +349,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   auto release = [&](int i, int c) {
     const int slot = i % NS;
     int* cnt = s_chunk + 2 * (slot * NCH + c);
-    __threadfence_block();
-    const int done = atomicAdd(cnt, 1) + 1;
-    __threadfence_block();
+    // acquire-release: this warp's reads of the chunk (ordered before the
+    // add by __syncwarp) come before whatever the last reader issues next
+    int done;
+    asm volatile("atom.add.acq_rel.cta.shared::cta.s32 %0, [%1], 1;"
+                 : "=r"(done)
+                 : "r"(smem_u32(cnt))
+                 : "memory");
+    ++done;
     if (done == READERS) {
       *cnt = 0;
       if (i + NS < nst && !s_flag[0]) {
