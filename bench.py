@@ -337,8 +337,11 @@ def run_gpu(args, ws, rank, local):
     clocks.lines = clocks.lines[max(0, n_before - 2):]
     barrier(ws)
     total_ms = ev0.elapsed_time(ev1)
+    per_m_samples = {M: [] for M, _, _ in graphs}
     for M, a, b in marks:
-        per_m[M] += a.elapsed_time(b)
+        dt = a.elapsed_time(b)
+        per_m[M] += dt
+        per_m_samples[M].append(dt)
     total_ms = max_over_ranks(total_ms, ws, dev)
     ms_per_step = total_ms / args.steps
     total_bytes = sum_over_ranks(bytes_per_step * args.steps, ws, dev)
@@ -359,8 +362,36 @@ def run_gpu(args, ws, rank, local):
     for M, _, items in graphs:
         b = sum(m.info()["weight_bytes"] for m, _, _ in items)
         t = per_m[M] / args.steps
+        xs = sorted(per_m_samples[M])
+        qt = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
+        med = statistics.median(xs)
+        # one verify pass = one call on one matrix (the model workload: the
+        # whole 64-layer sweep)
+        passes = 1 if args.workload == "model" else len(items)
         m_breakdown[str(M)] = {"ms": round(t, 5), "GBps": round(b / (t * 1e-3) / 1e9, 1),
-                               "pct_of_peak": round(100 * b / (t * 1e-3) / 1e9 / peak, 1)}
+                               "pct_of_peak": round(100 * b / (t * 1e-3) / 1e9 / peak, 1),
+                               "ms_median": round(med, 5), "ms_p10": round(qt(0.1), 5),
+                               "ms_p90": round(qt(0.9), 5),
+                               "GBps_median": round(b / (med * 1e-3) / 1e9, 1),
+                               "verify_passes_per_s": round(passes / (med * 1e-3), 1)}
+
+    # ---- one isolated call per M after an L2 flush (a 2 x L2 buffer written
+    # first; the events bracket the call only): no neighbour to overlap with
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for M, _, items in graphs:
+        m0, act0, out0 = items[0]
+        iso = []
+        for _ in range(5):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            q.qmm_verify(m0.handle, act0, out0, act0.shape[0])
+            b.record(stream)
+            torch.cuda.synchronize()
+            iso.append(a.elapsed_time(b) * 1e3)
+        m_breakdown[str(M)]["isolated_call_us"] = round(statistics.median(iso), 2)
+    del flush
 
     # ---- end to end through the host-buffer entry point (pinned buffers)
     e2e = None
