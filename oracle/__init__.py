@@ -18,6 +18,8 @@ Pin status (what fixes each function other than itself; see tests/test_oracle_pi
   FWHT (fp32 and fp64)         -- H H^T = 32 I, unit vectors, involution, fp64 bound
   verify product               -- M independent GEMVs, brute force vs numpy and exact
                                   rationals, one-hot and all-ones special cases
+  greedy acceptance            -- hand-worked cases (tests/golden/greedy_accept.json),
+                                  numpy's first-occurrence argmax, brute-force prefix
 """
 from __future__ import annotations
 
@@ -32,7 +34,7 @@ __all__ = [
     "lib", "bf16_to_f64", "f16_to_f64", "e4m3_to_f64", "f32_to_f16_rne", "f32_to_e4m3_sat",
     "fwht32_f32", "fwht32_f64", "hadamard32_act_f32", "q4_0_quantize", "q4_0_quantize_h32",
     "q4_0_dequant", "fp8_quantize", "fp8_dequant", "matmul_f64", "verify_rows",
-    "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8",
+    "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8", "greedy_accept",
 ]
 
 FMT_Q4_0 = 0
@@ -57,6 +59,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
     L.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
     L.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    L.oracle_greedy_accept.restype = _INT
+    L.oracle_greedy_accept.argtypes = [_P, _I64, _INT, _I64, _P, _P, _P]
     L.oracle_fwht32_f32.argtypes = [_P, _P]
     L.oracle_fwht32_f64.argtypes = [_P, _P]
     L.oracle_hadamard32_act_f32.argtypes = [_P, _I64, _INT, _I64, _P]
@@ -245,6 +249,25 @@ def verify_rows(fmt: int, wbytes: np.ndarray, scales, N: int, K: int, act_bf16: 
     if rc != 0:
         raise ValueError(f"oracle_verify_rows failed with {rc}")
     return out, S
+
+
+def greedy_accept(logits: np.ndarray, tokens: np.ndarray):
+    """Greedy acceptance of a verified block: (argmax [M] int32, k, next token).
+
+    ``logits`` [M][N] fp64 scores of the M block positions; ``tokens`` [M] the
+    block's input tokens (tokens[0] the last committed one).  See
+    ``oracle_greedy_accept`` in qmm_oracle.c.
+    """
+    lg = _c(logits, np.float64)
+    tk = _c(tokens, np.int32)
+    M, N = lg.shape
+    assert tk.shape == (M,)
+    am = np.empty(M, np.int32)
+    res = np.empty(2, np.int32)
+    rc = lib().oracle_greedy_accept(_ptr(lg), N, M, N, _ptr(tk), _ptr(am), _ptr(res))
+    if rc != 0:
+        raise ValueError(f"oracle_greedy_accept failed with {rc}")
+    return am, int(res[0]), int(res[1])
 
 
 def num_threads() -> int:

@@ -375,10 +375,44 @@ def check_hadamard_act_model(O):
             assert (np.abs(got[m, 32 * b:32 * b + 32] - ref) <= bound).all()
 
 
+# ---------------------------------------------------------------- greedy acceptance
+def check_greedy_golden(O):
+    """Hand-worked blocks (tests/golden/greedy_accept.json)."""
+    for case in _golden("greedy_accept.json")["cases"]:
+        lg = np.array(case["logits"], np.float64)
+        am, k, nxt = O.greedy_accept(lg, np.array(case["tokens"], np.int32))
+        assert am.tolist() == case["argmax"], case["name"]
+        assert (k, nxt) == (case["k"], case["next"]), case["name"]
+
+
+def check_greedy_vs_library(O):
+    """Argmax against numpy's (first occurrence of the maximum), on scores
+    rounded coarsely so that ties are frequent; k against a brute-force count
+    of the leading agreements, with drafts built to agree up to a chosen
+    position."""
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        M = int(rng.integers(1, 17))
+        N = int(rng.integers(1, 40))
+        lg = np.round(rng.standard_normal((M, N)) * 2.0) / 2.0
+        ref = np.argmax(lg, axis=1).astype(np.int32)
+        j = int(rng.integers(0, M))  # drafts agree at positions < j
+        tokens = rng.integers(0, N, M).astype(np.int32)
+        tokens[1:j + 1] = ref[:j]
+        if j + 1 < M and N > 1 and tokens[j + 1] == ref[j]:
+            tokens[j + 1] = (ref[j] + 1) % N
+        am, k, nxt = O.greedy_accept(lg, tokens)
+        assert (am == ref).all()
+        agree = (ref[:-1] == tokens[1:]) if M > 1 else np.zeros(0, bool)
+        kk = int(np.cumprod(agree).sum()) if M > 1 else 0
+        assert k == kk and nxt == ref[kk]
+        assert k == (j if N > 1 else M - 1) or N == 1
+
+
 ALL_CHECKS = [
     check_bf16_decode, check_f16_decode, check_e4m3_decode, check_f16_encode,
     check_e4m3_encode, check_q4_0_dequant_closed_form, check_top_bit_flip,
     check_q4_0_quantizer, check_fp8_quantizer, check_hadamard, check_rotated_product,
     check_product_brute_force, check_rows_are_independent_gemvs, check_special_activations,
-    check_hadamard_act_model,
+    check_hadamard_act_model, check_greedy_golden, check_greedy_vs_library,
 ]

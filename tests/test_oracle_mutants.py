@@ -49,6 +49,11 @@ MUTANTS = [
     ("product_sabs_signed", "            sabs += fabs(p);\n          }\n          out[(int64_t)m * nrows + i]",
      "            sabs += p;\n          }\n          out[(int64_t)m * nrows + i]", None),
     ("product_wrong_act_row", "double p = a[(int64_t)m * K + k] * w[k];", "double p = a[(int64_t)(M - 1 - m) * K + k] * w[k];", None),
+    ("greedy_last_tie", "if (row[n] > row[best]) best = n;", "if (row[n] >= row[best]) best = n;", None),
+    ("greedy_argmin", "if (row[n] > row[best]) best = n;", "if (row[n] < row[best]) best = n;", None),
+    ("greedy_token_offset", "argmax[k] == tokens[k + 1]", "argmax[k] == tokens[k]", None),
+    ("greedy_k_short", "while (k < M - 1 && argmax", "while (k < M - 2 && argmax", None),
+    ("greedy_next_is_last_draft", "result[1] = argmax[k];", "result[1] = argmax[k > 0 ? k - 1 : 0];", None),
     ("fp8_scale_tile_transposed", "double s = (double)scales[(n / 128) * tk_n + k / 128];",
      "double s = (double)scales[(n / 128) * tk_n + (k / 128 + n / 128) % tk_n];", None),
 ]
