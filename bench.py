@@ -10,7 +10,9 @@ programmatic dependent launch) and timed with CUDA events on the launching
 stream.  value = compressed weight bytes streamed per step / step time.
 
 Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h,
-fp8_mlp, model (64 layers x {qkv, out, gate+up, down}).
+fp8_mlp, model (64 layers x {qkv, out, gate+up, down}), q4_lmhead (the
+151,936 x 5120 output head through qmm_verify_greedy: the verify product plus
+the argmax and accepted-prefix step).
 
 Multi-GPU (--gpus N under torchrun): the path shards into independent
 problems, so every rank runs its own replica of the workload with no
@@ -49,6 +51,8 @@ WORKLOADS = {
     "q4_gateup_h": ("q4_gateup", True, (16,)),
     "q4_down_h": ("q4_down", True, (16,)),
     "fp8_mlp": ("fp8_mlp", False, (1, 8, 16)),
+    # output head with the greedy acceptance step (qmm_verify_greedy)
+    "q4_lmhead": ("q4_lmhead", False, (1, 8, 16)),
 }
 
 
@@ -291,9 +295,27 @@ def run_gpu(args, ws, rank, local):
         main_kernel = "verify_kernel<" + ("0" if spec["fmt"] == "q4_0" else "1")
         dtype = "f16" if (hadamard or spec["fmt"] != "q4_0") else "bf16"
 
+    # the greedy workload: per call the block's tokens (shared per M) and its
+    # argmax [M] and accept [2] outputs, in one int32 buffer per M
+    greedy = args.workload == "q4_lmhead"
+    gbufs = {}
+    if greedy:
+        for M, items in groups:
+            tok = torch.zeros(M, dtype=torch.int32, device=dev)
+            res = torch.zeros((len(items), M + 2), dtype=torch.int32, device=dev)
+            gbufs[M] = (tok, res)
+
+    def call(m, act, out, j=0):
+        M = act.shape[0]
+        if greedy:
+            tok, res = gbufs[M]
+            q.qmm_verify_greedy(m.handle, act, out, M, tok, res[j, :M], res[j, M:])
+        else:
+            q.qmm_verify(m.handle, act, out, M)
+
     def run_group(items):
-        for m, act, out in items:
-            q.qmm_verify(m.handle, act, out, act.shape[0])
+        for j, (m, act, out) in enumerate(items):
+            call(m, act, out, j)
 
     graphs = [(M, capture(torch, lambda it=items: run_group(it)), items) for M, items in groups]
     # kernels per call: the verify kernel, plus the activation pre-pass on the f16 paths
@@ -391,7 +413,7 @@ def run_gpu(args, ws, rank, local):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            q.qmm_verify(m0.handle, act0, out0, act0.shape[0])
+            call(m0, act0, out0)
             b.record(stream)
             torch.cuda.synchronize()
             iso.append(a.elapsed_time(b) * 1e3)
@@ -410,19 +432,23 @@ def run_gpu(args, ws, rank, local):
             for _, act, _ in items:
                 if all(act.data_ptr() != d.data_ptr() for d, _ in ins):
                     ins.append((act, act.cpu().pin_memory()))
+            if greedy:  # the step's result is the decision: argmax and accepted count per call
+                dev_out = gbufs[M][1].view(-1)
+                plan.append((ins, items, dev_out, torch.empty(dev_out.numel(), dtype=torch.int32).pin_memory()))
+                continue
             base = items[0][2]
             n_out = sum(out.numel() for _, _, out in items)
             dev_out = torch.as_strided(base, (n_out,), (1,))  # the contiguous buffer behind the views
             plan.append((ins, items, dev_out, torch.empty(n_out, dtype=torch.float32).pin_memory()))
         h2d = sum(hi.numel() * 2 for ins, _, _, _ in plan for _, hi in ins)
-        d2h = sum(ho.numel() * 4 for _, _, _, ho in plan)
+        d2h = sum(ho.numel() * ho.element_size() for _, _, _, ho in plan)
 
         def e2e_step():
             for ins, items, dev_out, host_out in plan:
                 for d, hi in ins:
                     d.copy_(hi, non_blocking=True)
-                for m, act, out in items:
-                    q.qmm_verify(m.handle, act, out, act.shape[0])
+                for j, (m, act, out) in enumerate(items):
+                    call(m, act, out, j)
                 host_out.copy_(dev_out, non_blocking=True)
             torch.cuda.synchronize()
 

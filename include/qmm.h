@@ -155,6 +155,34 @@ int qmm_destroy(qmm_t h);
 int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
                int M, void* stream);
 
+/* The verify product followed by greedy acceptance of the drafted block, the
+ * step that decides what is committed ["Qwen3.8-27B on the AMD R9700: up to
+ * 227 tok/s", sections "A block-diffusion drafter, verified exactly" and
+ * "What 'lossless' means here, precisely": every drafted token is checked
+ * against the target's own greedy choice and the agreeing prefix is kept].
+ * W is the output head (N = vocabulary size) and act the M block positions'
+ * final hidden rows.  Computes out exactly as qmm_verify, and then
+ *   argmax[m] = the first n with out[m][n] == max_n out[m][n] (a NaN counts
+ *               as larger than every number; -0 and +0 are equal),
+ *   accept[0] = k, the largest k <= M - 1 with argmax[m] == tokens[m + 1]
+ *               for every m < k (the number of accepted drafts),
+ *   accept[1] = argmax[k], the target's own token after them.
+ *   tokens : device, int32 [M]: the block's input tokens; tokens[0] is the
+ *            last committed token, tokens[1..M-1] the drafts.
+ *   argmax : device, int32 [M], written.   accept : device, int32 [2], written.
+ * The argmax is taken inside the verify kernel: every finished row tile folds
+ * its best (score, row) pair into a per-handle maximum with one atomic, and
+ * the last tile to finish writes argmax and accept, so the result needs no
+ * second pass over the scores.  Because row results are bit-identical for every
+ * M, so is argmax: a batched verify of M positions picks the same tokens as M
+ * single-row calls.  Asynchronous on `stream`, like qmm_verify; the handle's
+ * greedy state is per handle (one stream at a time).
+ * Errors: as qmm_verify, plus INVALID_ARG (NULL tokens/argmax/accept, or a
+ * handle created with QMM_FLAG_TCGEN05) and ALIGN (tokens/argmax/accept not
+ * 4-byte aligned). */
+int qmm_verify_greedy(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+                      const int32_t* tokens, int32_t* argmax, int32_t* accept, void* stream);
+
 /* The same product for callers that hold host buffers: copies act to the
  * handle's device staging buffer, runs qmm_verify, copies the result back into
  * out_host and waits for `stream` before returning (synchronous).  Pinned

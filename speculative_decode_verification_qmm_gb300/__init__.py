@@ -20,7 +20,8 @@ from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
-    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_host", "qmm_verify_noalloc", "qmm_sync_status",
+    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_greedy", "qmm_verify_host",
+    "qmm_verify_noalloc", "qmm_sync_status",
     "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
     "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
     "QmmError", "load",
@@ -99,6 +100,15 @@ def qmm_verify(h, act, out, M: int, stream=None) -> None:
     """act: CUDA bf16 [M, lda>=K]; out: CUDA fp32 [M, ldo>=N]; asynchronous."""
     _check("qmm_verify", load().qmm_verify(h, _ptr(act), act.stride(0), _ptr(out), out.stride(0),
                                            M, _stream_ptr(stream)))
+
+
+def qmm_verify_greedy(h, act, out, M: int, tokens, argmax, accept, stream=None) -> None:
+    """qmm_verify plus greedy acceptance: tokens CUDA int32 [M] (tokens[0] the
+    last committed token); argmax CUDA int32 [M] and accept CUDA int32 [2]
+    (accepted drafts, next token) are written; asynchronous."""
+    _check("qmm_verify_greedy", load().qmm_verify_greedy(
+        h, _ptr(act), act.stride(0), _ptr(out), out.stride(0), M, _ptr(tokens), _ptr(argmax),
+        _ptr(accept), _stream_ptr(stream)))
 
 
 def qmm_verify_host(h, act, out, M: int, stream=None) -> None:
@@ -214,6 +224,17 @@ class Matrix:
         w = torch.empty((self.N, self.K), dtype=torch.float32, device="cuda")
         qmm_dequantize(self.handle, w, stream)
         return w
+
+    def verify_greedy(self, act, tokens, out=None, stream=None):
+        """(out, argmax, accept) for the drafted block; see qmm_verify_greedy."""
+        import torch
+        M = act.shape[0]
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.float32, device=act.device)
+        argmax = torch.empty(M, dtype=torch.int32, device=act.device)
+        accept = torch.empty(2, dtype=torch.int32, device=act.device)
+        qmm_verify_greedy(self.handle, act, out, M, tokens, argmax, accept, stream)
+        return out, argmax, accept
 
     def info(self) -> dict:
         return qmm_get_info(self.handle)

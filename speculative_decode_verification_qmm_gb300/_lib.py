@@ -72,6 +72,7 @@ SIGNATURES = {
     "qmm_create": (_INT, [ctypes.POINTER(_P), ctypes.POINTER(qmm_desc), _P]),
     "qmm_destroy": (_INT, [_P]),
     "qmm_verify": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
+    "qmm_verify_greedy": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P, _P, _P, _P]),
     "qmm_verify_host": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
     "qmm_verify_noalloc": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
     "qmm_sync_status": (_INT, [_P, _P]),

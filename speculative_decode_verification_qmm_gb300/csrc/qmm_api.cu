@@ -19,6 +19,7 @@ namespace {
 
 constexpr uint64_t HANDLE_MAGIC = 0x514D4D5645524946ull;  // "QMMVERIF"
 constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+constexpr size_t GREEDY_STATE_BYTES = MAX_M * sizeof(unsigned long long) + 16;
 
 // Planner constants (they only rank candidate plans; see make_plan()): HBM
 // copy bandwidth of the part; tcgen05 kernel: what one CTA with its pipeline
@@ -60,6 +61,9 @@ struct qmm_handle {
   float* ws = nullptr;         // mma.sync kernels, S > 1: split partials
   int* counters = nullptr;     // mma.sync kernels, S > 1: [n_tiles] arrivals
   int* status = nullptr;       // device error word
+  // greedy acceptance state: [MAX_M] running maxima, then the finished-tile
+  // count (zero between calls)
+  unsigned long long* greedy = nullptr;
   uint16_t* stage_act = nullptr;  // host-buffer path: [MAX_M][act_pitch]
   int64_t stage_act_pitch = 0;
   float* stage_out = nullptr;     // [MAX_M][N]
@@ -190,6 +194,7 @@ void free_handle(qmm_handle* h) {
   cudaFree(h->ws);
   cudaFree(h->counters);
   cudaFree(h->status);
+  cudaFree(h->greedy);
   cudaFree(h->stage_act);
   cudaFree(h->stage_out);
   if (old >= 0 && old != h->device) cudaSetDevice(old);
@@ -396,6 +401,7 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
     QMM_ALLOC(h->counters, (size_t)p.n_tiles * sizeof(int));
   }
   QMM_ALLOC(h->status, sizeof(int));
+  QMM_ALLOC(h->greedy, GREEDY_STATE_BYTES);
   QMM_ALLOC(h->stage_act, (size_t)MAX_M * h->stage_act_pitch * sizeof(uint16_t));
   QMM_ALLOC(h->stage_out, (size_t)MAX_M * d->N * sizeof(float));
 
@@ -422,6 +428,7 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   if (e != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->act_scratch, 0, h->act_bytes, st)) != cudaSuccess) goto fail;
   if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
+  if ((e = cudaMemsetAsync(h->greedy, 0, GREEDY_STATE_BYTES, st)) != cudaSuccess) goto fail;
   if (h->counters &&
       (e = cudaMemsetAsync(h->counters, 0, (size_t)p.n_tiles * sizeof(int), st)) != cudaSuccess)
     goto fail;
@@ -453,11 +460,25 @@ int qmm_destroy(qmm_t h) {
   return QMM_OK;
 }
 
-int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
-               void* stream) {
+}  // extern "C"
+
+namespace {
+
+struct GreedyArgs {
+  const int32_t* tokens;
+  int32_t* argmax;
+  int32_t* accept;
+};
+
+// qmm_verify, and qmm_verify_greedy when `g` is not NULL.
+int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+                void* stream, const GreedyArgs* g) {
   if (!is_live(h)) return QMM_ERR_STATE;
   if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
   if (!act || !out) return QMM_ERR_INVALID_ARG;
+  if (g && (!g->tokens || !g->argmax || !g->accept || h->plan.tc)) return QMM_ERR_INVALID_ARG;
+  if (g && (((uintptr_t)g->tokens | (uintptr_t)g->argmax | (uintptr_t)g->accept) & 3))
+    return QMM_ERR_ALIGN;
   if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || lda < h->K || (lda & 7) || ldo < h->N)
     return QMM_ERR_ALIGN;
   int dev = -1;
@@ -466,7 +487,6 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   const Plan& p = h->plan;
   const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
   const bool f16 = had || h->fmt == 1;
-
   // bf16 operands read the caller's rows directly; the f16 paths (Hadamard
   // rotation, FP8) go through the activation pre-pass and its scratch.
   cudaError_t e = cudaSuccess;
@@ -501,6 +521,19 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
   vp.ws = h->ws;
   vp.counters = h->counters;
   vp.wait_limit_ns = h->wait_limit_ns;
+  vp.best = nullptr;
+  vp.tiles_done = nullptr;
+  vp.tokens = nullptr;
+  vp.argmax_out = nullptr;
+  vp.accept_out = nullptr;
+  vp.n_tiles = p.n_tiles;
+  if (g) {
+    vp.best = h->greedy;
+    vp.tiles_done = reinterpret_cast<int*>(h->greedy + MAX_M);
+    vp.tokens = g->tokens;
+    vp.argmax_out = g->argmax;
+    vp.accept_out = g->accept;
+  }
   VerifyLaunch vl;
   vl.fmt = h->fmt;
   vl.f16_ops = f16;
@@ -511,6 +544,22 @@ int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ld
           : launch_verify_kernel(h, vp, vl, act, lda, M, false);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+               void* stream) {
+  return verify_impl(h, act, lda, out, ldo, M, stream, nullptr);
+}
+
+int qmm_verify_greedy(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+                      const int32_t* tokens, int32_t* argmax, int32_t* accept, void* stream) {
+  GreedyArgs g{tokens, argmax, accept};
+  return verify_impl(h, act, lda, out, ldo, M, stream, &g);
 }
 
 int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_host, int64_t ldo,
@@ -736,6 +785,12 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   vp.ws = h->ws;
   vp.counters = h->counters;
   vp.wait_limit_ns = h->wait_limit_ns;
+  vp.best = nullptr;
+  vp.tiles_done = nullptr;
+  vp.tokens = nullptr;
+  vp.argmax_out = nullptr;
+  vp.accept_out = nullptr;
+  vp.n_tiles = p.n_tiles;
   VerifyLaunch vl;
   vl.fmt = h->fmt;
   vl.f16_ops = f16;

@@ -85,6 +85,13 @@ struct VerifyParams {
   float* ws;                 // mma.sync kernels, S > 1: [n_tiles][S][MAX_M][TILE_N] partials
   int* counters;             // mma.sync kernels, S > 1: [n_tiles] arrivals, zero between calls
   uint64_t wait_limit_ns;    // bounded waits give up after this (0: at once)
+  // Greedy acceptance (mma.sync kernels; best == NULL: plain verify).
+  unsigned long long* best;  // [MAX_M] largest (score key << 32 | ~row) so far, zero between calls
+  int* tiles_done;           // row tiles of the call finished, zero between calls
+  const int32_t* tokens;     // [M] the block's input tokens (tokens[0]: last committed)
+  int32_t* argmax_out;       // [M] first row of the largest score of each drafted row
+  int32_t* accept_out;       // [2] accepted drafts k, then argmax_out[k]
+  int n_tiles;               // row tiles of the call
 };
 
 struct PrepParams {

@@ -77,7 +77,10 @@ struct SmemLayout {
   // (the split partials go to the workspace in global memory)
   static constexpr int RED_PITCH = MAX_M + 2;  // floats per row
   static constexpr int RED_BYTES = STAGE_CHUNKS * TILE_N * RED_PITCH * 4;
-  static_assert(RED_BYTES <= NS * F::STAGE_BYTES, "the epilogue area must fit in the ring");
+  // then the finished tile [m][row] for the greedy epilogue
+  static constexpr int FIN_OFF = RED_BYTES;
+  static constexpr int FIN_BYTES = MAX_M * TILE_N * 4;
+  static_assert(FIN_OFF + FIN_BYTES <= NS * F::STAGE_BYTES, "the epilogue areas must fit in the ring");
   static_assert(A_OFF % 1024 == 0 && A_CHUNK % (F::CHUNK_K * 2 * 8) == 0,
                 "every box starts on a swizzle period");
   static_assert(F::CHUNK_BYTES % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
@@ -269,18 +272,92 @@ __device__ __forceinline__ void q4_chunk_simt(uint32_t unit, uint32_t achunk, in
 }
 
 // ---------------------------------------------------------------------------
+// Greedy acceptance, the step after the verify product: the target's greedy
+// token at every block position is the argmax of its row of scores, and the
+// drafts are accepted while they agree with it (see qmm_verify_greedy in
+// qmm.h).  Called by the CTA that finished row tile `tile` (its scores, times
+// the pre-pass multipliers, in fin[m][row]) with every thread.  For each
+// drafted row m the tile's best (score, row) pair joins the call-wide maximum
+// through one 64-bit atomicMax on a key that orders scores as floats and
+// equal scores by the lower row (so the result is the first index of the
+// maximum whatever order the tiles finish in; a NaN counts as the largest).
+// The last tile of the call to finish writes argmax_out, accept_out and clears
+// the state for the next call.  `valid` false (the CTA gave up on a wait): the
+// tile only counts its arrival.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long greedy_key(float v, int64_t row) {
+  uint32_t u = __float_as_uint(v + 0.0f);      // -0 -> +0
+  if (v != v) u = 0x7FC00000u;                 // every NaN as one positive NaN
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (uint32_t)~(uint32_t)row;
+}
+
+static __device__ __noinline__ void greedy_tile(const VerifyParams& p, const float* fin, int tile, int M,
+                                         bool valid, int tid, volatile int* flag) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (valid) {
+    // warp w: drafted rows w and w + 8; lane l: tile rows l, l + 32, l + 64, l + 96
+    for (int m = warp; m < M; m += THREADS / 32) {
+      unsigned long long best = 0;
+#pragma unroll
+      for (int r = 0; r < TILE_N / 32; ++r) {
+        const int row = lane + 32 * r;
+        const int64_t n = (int64_t)tile * TILE_N + row;
+        if (n < p.N) {
+          const unsigned long long k = greedy_key(fin[m * TILE_N + row], n);
+          best = k > best ? k : best;
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, d);
+        best = o > best ? o : best;
+      }
+      if (lane == 0 && best) atomicMax(p.best + m, best);
+    }
+  }
+  // One GPU-scope acquire-release add after the CTA barrier: it releases the
+  // maxima of this tile and, for the last tile, acquires every other tile's.
+  __syncthreads();
+  if (tid == 0) {
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(p.tiles_done)
+                 : "memory");
+    flag[3] = prev == p.n_tiles - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (flag[3] && tid == 0) {
+    *p.tiles_done = 0;
+    int32_t y[MAX_M];
+    for (int m = 0; m < M; ++m) {
+      const unsigned long long k = __ldcg(p.best + m);
+      y[m] = (int32_t)~(uint32_t)(k & 0xFFFFFFFFull);
+      p.argmax_out[m] = y[m];
+    }
+    int k = 0;
+    while (k < M - 1 && y[k] == p.tokens[k + 1]) ++k;
+    p.accept_out[0] = k;
+    p.accept_out[1] = y[k];
+    for (int m = 0; m < MAX_M; ++m) p.best[m] = 0ull;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 //   FMT  0 = Q4_0, 1 = FP8
 //   Op   Bf16Op or F16Op (FP8 always F16Op)
 //   NT8  1 for M <= 8, 2 for M <= 16 (R = 8 * NT8 activation rows staged)
 //   SIMT true: CUDA-core baseline compute (Q4_0 only)
 //   NS   pipeline depth in stages
+//   GREEDY  also the greedy acceptance step (p.best and the rest set)
 // `amap` is a 2-D tensor map over the 16-bit activation rows (see
 // qmm_common.cuh) whose boxes are CHUNK_K columns x R rows, swizzled by
 // 2 x CHUNK_K bytes.
 // ---------------------------------------------------------------------------
 // Two CTAs per SM: 16 warps, four per SM sub-partition, up to 128 registers.
-template <int FMT, typename Op, int NT8, bool SIMT, int NS>
+template <int FMT, typename Op, int NT8, bool SIMT, int NS, bool GREEDY>
 __global__ void __launch_bounds__(THREADS, 2)
     verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap amap) {
   using F = FmtTraits<FMT>;
@@ -510,6 +587,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // pre-pass's factor of this (row, split).  With one split it is the result;
   // otherwise it goes to the handle's workspace, [tile][split][m][row].
   float* mine = p.ws + ((int64_t)tile * p.S + split) * (MAX_M * TILE_N);
+  float* fin = reinterpret_cast<float*>(smem + L::W_OFF + L::FIN_OFF);  // [m][row], greedy only
   if (tid < TILE_N && !aborted) {
     constexpr int NRED = SIMT ? 1 : STAGE_CHUNKS;
     const int64_t n = (int64_t)tile * TILE_N + tid;
@@ -520,12 +598,19 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (p.out_scale) v *= p.out_scale[m * p.S + split];
       if (p.S == 1) {
         if (n < p.N) p.out[(int64_t)m * p.ldo + n] = v;
+        if constexpr (GREEDY) fin[m * TILE_N + tid] = v;
       } else {
         mine[m * TILE_N + tid] = v;
       }
     }
   }
-  if (p.S == 1) return;
+  if (p.S == 1) {
+    if constexpr (GREEDY) {
+      __syncthreads();  // fin complete
+      greedy_tile(p, fin, tile, M, !aborted, tid, s_flag);
+    }
+    return;
+  }
 
   // Split K: the last of the tile's S CTAs to arrive adds the S partials in
   // split order (the count goes back to zero for the next call).  Nobody
@@ -566,6 +651,14 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int64_t n = (int64_t)tile * TILE_N + row + r;
         if (n < p.N) p.out[(int64_t)m * p.ldo + n] = vals[r];
       }
+      if constexpr (GREEDY) *reinterpret_cast<float4*>(fin + m * TILE_N + row) = v;
+    }
+  }
+  // the tile is finished by its last split
+  if constexpr (GREEDY) {
+    if (s_flag[1]) {
+      __syncthreads();
+      greedy_tile(p, fin, tile, M, !aborted, tid, s_flag);
     }
   }
 }
