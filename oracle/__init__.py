@@ -15,7 +15,9 @@ Pin status (what fixes each function other than itself; see tests/test_oracle_pi
   encoders (fp16, e4m3)        -- exhaustive round trips, midpoint ties, library casts
   Q4_0 quantize / dequant      -- closed form, hand blocks, top-bit-flip identity, bounds
   FP8 quantize / dequant       -- closed form, library cast, tile bounds
-  FWHT (fp32 and fp64)         -- H H^T = 32 I, unit vectors, involution, fp64 bound
+  FWHT (fp32 and fp64)         -- H H^T = B I, unit vectors, involution, fp64 bound, the
+                                  closed-form ramp, and (B = 64, 128) the bit-exact
+                                  half-size recursion that fixes the stage order
   verify product               -- M independent GEMVs, brute force vs numpy and exact
                                   rationals, one-hot and all-ones special cases
   greedy acceptance            -- hand-worked cases (tests/golden/greedy_accept.json),
@@ -33,6 +35,7 @@ from . import build as _build
 __all__ = [
     "lib", "bf16_to_f64", "f16_to_f64", "e4m3_to_f64", "f32_to_f16_rne", "f32_to_e4m3_sat",
     "fwht32_f32", "fwht32_f64", "hadamard32_act_f32", "q4_0_quantize", "q4_0_quantize_h32",
+    "fwht_f32", "fwht_f64", "hadamard_act_f32", "rotate_weights_f32",
     "q4_0_dequant", "fp8_quantize", "fp8_dequant", "matmul_f64", "verify_rows",
     "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8", "greedy_accept",
 ]
@@ -59,6 +62,10 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
     L.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
     L.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    L.oracle_fwht_f32.argtypes = [_P, _P, _INT]
+    L.oracle_fwht_f64.argtypes = [_P, _P, _INT]
+    L.oracle_hadamard_act_f32.argtypes = [_P, _I64, _INT, _I64, _INT, _P]
+    L.oracle_rotate_weights_f32.argtypes = [_P, _I64, _I64, _INT, _P]
     L.oracle_greedy_accept.restype = _INT
     L.oracle_greedy_accept.argtypes = [_P, _I64, _INT, _I64, _P, _P, _P]
     L.oracle_fwht32_f32.argtypes = [_P, _P]
@@ -152,6 +159,54 @@ def fwht32_f64(x) -> np.ndarray:
     return out.reshape(v.shape)
 
 
+def fwht_f32(x, B: int) -> np.ndarray:
+    """fp32 device model of the unnormalised B-point transform (B = 32, 64, 128)
+    over the last axis."""
+    v = _c(x, np.float32)
+    assert B in (32, 64, 128) and v.shape[-1] == B
+    flat = v.reshape(-1, B)
+    out = np.empty_like(flat)
+    for i in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[i])
+        o = np.empty(B, np.float32)
+        lib().oracle_fwht_f32(_ptr(row), _ptr(o), B)
+        out[i] = o
+    return out.reshape(v.shape)
+
+
+def fwht_f64(x, B: int) -> np.ndarray:
+    v = _c(x, np.float64)
+    assert B in (32, 64, 128) and v.shape[-1] == B
+    flat = v.reshape(-1, B)
+    out = np.empty_like(flat)
+    for i in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[i])
+        o = np.empty(B, np.float64)
+        lib().oracle_fwht_f64(_ptr(row), _ptr(o), B)
+        out[i] = o
+    return out.reshape(v.shape)
+
+
+def hadamard_act_f32(act_bf16: np.ndarray, B: int) -> np.ndarray:
+    """fp32 device model of the B-block activation rotation: [M][K] bf16 bits -> fp32."""
+    a = _c(act_bf16, np.uint16)
+    M, K = a.shape
+    assert B in (32, 64, 128) and K % B == 0
+    out = np.empty((M, K), np.float32)
+    lib().oracle_hadamard_act_f32(_ptr(a), K, M, K, B, _ptr(out))
+    return out
+
+
+def rotate_weights_f32(w: np.ndarray, B: int) -> np.ndarray:
+    """The offline weight rotation: every B-block of a row rotated (fp32) and times 1/B."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert B in (32, 64, 128) and K % B == 0
+    out = np.empty((N, K), np.float32)
+    lib().oracle_rotate_weights_f32(_ptr(w), N, K, B, _ptr(out))
+    return out
+
+
 def hadamard32_act_f32(act_bf16: np.ndarray) -> np.ndarray:
     """fp32 device model of the activation rotation: [M][K] bf16 bits -> [M][K] fp32."""
     a = _c(act_bf16, np.uint16)
@@ -225,8 +280,18 @@ def matmul_f64(act: np.ndarray, w: np.ndarray, want_s: bool = True):
     return (out, S) if want_s else out
 
 
+def _hb(hadamard) -> int:
+    """Rotation block size from False / True (32) / 32 / 64 / 128."""
+    if hadamard is True:
+        return 32
+    if not hadamard:
+        return 0
+    assert int(hadamard) in (32, 64, 128)
+    return int(hadamard)
+
+
 def verify_rows(fmt: int, wbytes: np.ndarray, scales, N: int, K: int, act_bf16: np.ndarray,
-                hadamard: bool = False, rows=None):
+                hadamard=False, rows=None):
     """Verify product for selected weight rows (all rows when ``rows`` is None).
 
     Returns (out [M][len(rows)], S [M][len(rows)]) in fp64.
@@ -244,7 +309,7 @@ def verify_rows(fmt: int, wbytes: np.ndarray, scales, N: int, K: int, act_bf16: 
     out = np.empty((M, nr), np.float64)
     S = np.empty((M, nr), np.float64)
     rc = lib().oracle_verify_rows(fmt, _ptr(wb), _ptr(sc) if sc is not None else None, N, K,
-                                  _ptr(a), lda, M, int(bool(hadamard)),
+                                  _ptr(a), lda, M, _hb(hadamard),
                                   _ptr(r) if r is not None else None, nr, _ptr(out), _ptr(S))
     if rc != 0:
         raise ValueError(f"oracle_verify_rows failed with {rc}")

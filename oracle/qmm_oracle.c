@@ -160,50 +160,79 @@ uint8_t oracle_f32_to_e4m3_sat(float xf) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* 32-point Walsh-Hadamard transform.                                         */
+/* Walsh-Hadamard transforms of B = 32, 64 or 128 points.                     */
 /* ------------------------------------------------------------------------ */
 
-/* fp32 device model: strides 1,2,4,8,16; every stage maps (x, y) to
- * (x + y, x - y) for the index pairs (i, i + h) with (i & h) == 0. */
-void oracle_fwht32_f32(const float* in, float* out) {
-  float v[32];
-  for (int i = 0; i < 32; ++i) v[i] = in[i];
-  for (int h = 1; h < 32; h <<= 1) {
-    for (int i = 0; i < 32; ++i) {
+/* fp32 device model of the unnormalised B-point transform (H H^T = B I):
+ * strides 1, 2, 4, ..., B/2; every stage maps (x, y) to (x + y, x - y) for the
+ * index pairs (i, i + h) with (i & h) == 0.  For B = 32 this is the stage
+ * order of the page's 32-point rotation ["Qwen3.8-27B at 45.7 tok/s: DFlash2
+ * in 1bit serve, and 4-bit activations with a Hadamard rotation", section
+ * "Prompt processing: 4-bit activations, rotated first"]; the larger sizes,
+ * which the page lists as the next step ("What's next"), keep the same
+ * stride-ascending order (a reading: the page gives none for them). */
+void oracle_fwht_f32(const float* in, float* out, int B) {
+  float v[128];
+  for (int i = 0; i < B; ++i) v[i] = in[i];
+  for (int h = 1; h < B; h <<= 1) {
+    for (int i = 0; i < B; ++i) {
       if (i & h) continue;
       float x = v[i], y = v[i + h];
       v[i] = x + y;
       v[i + h] = x - y;
     }
   }
-  for (int i = 0; i < 32; ++i) out[i] = v[i];
+  for (int i = 0; i < B; ++i) out[i] = v[i];
 }
 
-/* Same butterflies in fp64 (exact for inputs with <= 48 significant bits). */
-void oracle_fwht32_f64(const double* in, double* out) {
-  double v[32];
-  for (int i = 0; i < 32; ++i) v[i] = in[i];
-  for (int h = 1; h < 32; h <<= 1) {
-    for (int i = 0; i < 32; ++i) {
+/* Same butterflies in fp64 (exact for inputs with <= 46 significant bits). */
+void oracle_fwht_f64(const double* in, double* out, int B) {
+  double v[128];
+  for (int i = 0; i < B; ++i) v[i] = in[i];
+  for (int h = 1; h < B; h <<= 1) {
+    for (int i = 0; i < B; ++i) {
       if (i & h) continue;
       double x = v[i], y = v[i + h];
       v[i] = x + y;
       v[i + h] = x - y;
     }
   }
-  for (int i = 0; i < 32; ++i) out[i] = v[i];
+  for (int i = 0; i < B; ++i) out[i] = v[i];
 }
 
-/* Rotate every 32-block of M bf16 activation rows with the fp32 model.
- * act: [M][lda] bf16 bits; out: [M][K] fp32.  K must be a multiple of 32. */
+void oracle_fwht32_f32(const float* in, float* out) { oracle_fwht_f32(in, out, 32); }
+void oracle_fwht32_f64(const double* in, double* out) { oracle_fwht_f64(in, out, 32); }
+
+/* Rotate every B-block of M bf16 activation rows with the fp32 model.
+ * act: [M][lda] bf16 bits; out: [M][K] fp32.  K must be a multiple of B. */
+void oracle_hadamard_act_f32(const uint16_t* act, int64_t lda, int M, int64_t K, int B,
+                             float* out) {
+  for (int m = 0; m < M; ++m) {
+    for (int64_t b = 0; b < K / B; ++b) {
+      float blk[128];
+      for (int j = 0; j < B; ++j)
+        blk[j] = (float)oracle_bf16_to_f64(act[(int64_t)m * lda + B * b + j]);
+      oracle_fwht_f32(blk, out + (int64_t)m * K + B * b, B);
+    }
+  }
+}
+
 void oracle_hadamard32_act_f32(const uint16_t* act, int64_t lda, int M, int64_t K,
                                float* out) {
-  for (int m = 0; m < M; ++m) {
-    for (int64_t b = 0; b < K / 32; ++b) {
-      float blk[32];
-      for (int j = 0; j < 32; ++j)
-        blk[j] = (float)oracle_bf16_to_f64(act[(int64_t)m * lda + 32 * b + j]);
-      oracle_fwht32_f32(blk, out + (int64_t)m * K + 32 * b);
+  oracle_hadamard_act_f32(act, lda, M, K, 32, out);
+}
+
+/* The offline weight rotation of the B-block variants: every B-block of a
+ * weight row is rotated with the fp32 butterflies and multiplied by 1/B (a
+ * power of two, exact).  out: [N][K] fp32. */
+void oracle_rotate_weights_f32(const float* w, int64_t N, int64_t K, int B, float* out) {
+  const float inv_b = 1.0f / (float)B;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < K / B; ++b) {
+      float* r = out + n * K + B * b;
+      oracle_fwht_f32(w + n * K + B * b, r, B);
+      for (int j = 0; j < B; ++j) r[j] = r[j] * inv_b;
     }
   }
 }
@@ -355,18 +384,20 @@ void oracle_matmul_f64(const double* act, const double* w, int M, int64_t N, int
   }
 }
 
-/* Decode the bf16 activation rows to fp64; in the Hadamard variant rotate each
- * 32-block exactly in fp64 (sums of 32 bf16 values are exact in fp64). */
+/* Decode the bf16 activation rows to fp64; in the Hadamard variants rotate
+ * each B-block exactly in fp64 (sums of up to 128 bf16 values are exact in
+ * fp64).  hadamard: 0 none, 1 or 32, 64, 128 = the block size B. */
 static void decode_act(const uint16_t* act, int64_t lda, int M, int64_t K, int hadamard,
                        double* a) {
   for (int m = 0; m < M; ++m)
     for (int64_t k = 0; k < K; ++k)
       a[(int64_t)m * K + k] = oracle_bf16_to_f64(act[(int64_t)m * lda + k]);
+  const int B = hadamard == 1 ? 32 : hadamard;
   if (hadamard) {
     for (int m = 0; m < M; ++m)
-      for (int64_t b = 0; b < K / 32; ++b) {
-        double* blk = a + (int64_t)m * K + 32 * b;
-        oracle_fwht32_f64(blk, blk);
+      for (int64_t b = 0; b < K / B; ++b) {
+        double* blk = a + (int64_t)m * K + B * b;
+        oracle_fwht_f64(blk, blk, B);
       }
   }
 }
@@ -379,7 +410,9 @@ static void decode_act(const uint16_t* act, int64_t lda, int M, int64_t K, int h
 int oracle_verify_rows(int fmt, const uint8_t* wbytes, const float* scales, int64_t N,
                        int64_t K, const uint16_t* act, int64_t lda, int M, int hadamard,
                        const int64_t* rows, int64_t nrows, double* out, double* S) {
-  if (K <= 0 || N <= 0 || M <= 0 || (fmt == 0 && K % 32) || (hadamard && K % 32))
+  const int hb = hadamard == 1 ? 32 : hadamard;
+  if (K <= 0 || N <= 0 || M <= 0 || (fmt == 0 && K % 32) ||
+      (hb && ((hb != 32 && hb != 64 && hb != 128) || K % hb)))
     return -1;
   if (!rows) nrows = N;
   double* a = (double*)malloc(sizeof(double) * (size_t)M * (size_t)K);

@@ -262,6 +262,52 @@ def check_hadamard(O):
     assert (np.abs(got - ref) <= bound).all()
 
 
+def sylvester(B: int) -> np.ndarray:
+    """Closed-form unnormalised Sylvester matrix of size B, H[j][i] = (-1)^popcount(i & j)."""
+    i = np.arange(B)
+    pc = np.vectorize(lambda v: bin(int(v)).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1, -1).astype(np.int64)
+
+
+def check_hadamard_larger(O):
+    """The 64- and 128-point transforms: closed forms, the involution, the fp32
+    error bound, and a bit-exact recursion that fixes the stage order: with
+    strides ascending, the B-point fp32 result is (A + C, A - C) in fp32 where
+    A and C are the B/2-point results of the two halves (so B = 64 rests on the
+    pinned 32-point transform, and B = 128 on B = 64)."""
+    rng = np.random.default_rng(19)
+    for B in (64, 128):
+        H = sylvester(B)
+        assert (H @ H.T == B * np.eye(B, dtype=np.int64)).all()
+        eye = np.eye(B)
+        assert (O.fwht_f64(eye, B) == H.T.astype(np.float64)).all()
+        assert (O.fwht_f32(eye.astype(np.float32), B) == H.T.astype(np.float32)).all()
+        # ramp x_i = i + 1: (Hx)_0 = B (B + 1) / 2, (Hx)_j = -(B / 2) j for j a
+        # power of two, 0 otherwise (worked by hand from the bits of i)
+        x = np.arange(1, B + 1, dtype=np.float64)
+        want = np.zeros(B)
+        want[0] = B * (B + 1) / 2
+        for b in range(int(np.log2(B))):
+            want[1 << b] = -(B / 2) * (1 << b)
+        assert (O.fwht_f64(x, B) == want).all() and (O.fwht_f32(x.astype(np.float32), B) == want).all()
+        v = rng.standard_normal((100, B)).astype(np.float32).astype(np.float64)
+        assert (O.fwht_f64(O.fwht_f64(v, B), B) == B * v).all()
+        v32 = (rng.standard_normal((300, B)) * 10.0 ** rng.uniform(-3, 3, (300, 1))).astype(np.float32)
+        got = O.fwht_f32(v32, B)
+        ref = v32.astype(np.float64) @ H.T.astype(np.float64)
+        bound = (np.log2(B) + 1) * 2.0 ** -24 * np.abs(v32.astype(np.float64)).sum(axis=1, keepdims=True)
+        assert (np.abs(got.astype(np.float64) - ref) <= bound).all()
+        h = B // 2
+        A = O.fwht_f32(v32[:, :h], h) if h > 32 else O.fwht32_f32(v32[:, :h])
+        C = O.fwht_f32(v32[:, h:], h) if h > 32 else O.fwht32_f32(v32[:, h:])
+        rec = np.concatenate([A + C, A - C], axis=1)  # fp32 adds, round to nearest even
+        assert (got == rec).all(), B
+        # the activation rotation and the offline weight rotation use the same model
+        a = (rng.standard_normal((3, 2 * B)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        af = (a.astype(np.uint32) << 16).view(np.float32)
+        assert (O.hadamard_act_f32(a, B) == O.fwht_f32(af.reshape(3, 2, B), B).reshape(3, 2 * B)).all()
+
+
 def check_rotated_product(O):
     """Rotated activations times rotated (offline, /32) weights equal the
     activations times the un-rotated dequantized weights H^T deq(w')."""
@@ -285,6 +331,29 @@ def check_rotated_product(O):
 
 
 # ---------------------------------------------------------------- product
+def check_rotated_product_larger(O):
+    """B = 64, 128: rotated activations times weights rotated offline (fp32,
+    times 1/B) and quantized equal the activations times the un-rotated
+    dequantized weights H^T deq(w') / (1) -- H H^T = B I and the 1/B in the
+    weights cancel."""
+    import speculative_decode_verification_qmm_gb300.synth as synth
+    N, K, M = 40, 256, 4
+    for B in (64, 128):
+        H = sylvester(B).astype(np.float64)
+        w = synth.weights(N, K, 23 + B)
+        a = synth.activations(M, K, 24 + B, outliers=True)
+        wr = O.rotate_weights_f32(w, B)
+        blocks = O.q4_0_quantize(wr)
+        out_rot, _ = O.verify_rows(O.FMT_Q4_0, blocks, None, N, K, a, hadamard=B)
+        wq = O.q4_0_dequant(blocks, N, K)
+        w_un = (wq.reshape(N, K // B, B) @ H).reshape(N, K)
+        af = synth.bf16_bits_to_f32(a).astype(np.float64)
+        ref = af @ w_un.T
+        assert np.allclose(out_rot, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+        rel = np.linalg.norm(w_un - w) / np.linalg.norm(w)
+        assert rel < 0.2, rel
+
+
 def check_product_brute_force(O):
     import speculative_decode_verification_qmm_gb300.synth as synth
     for (M, K, N) in ((4, 32, 64), (4, 64, 32)):
@@ -415,4 +484,5 @@ ALL_CHECKS = [
     check_q4_0_quantizer, check_fp8_quantizer, check_hadamard, check_rotated_product,
     check_product_brute_force, check_rows_are_independent_gemvs, check_special_activations,
     check_hadamard_act_model, check_greedy_golden, check_greedy_vs_library,
+    check_hadamard_larger, check_rotated_product_larger,
 ]

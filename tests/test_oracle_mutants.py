@@ -38,10 +38,14 @@ MUTANTS = [
     ("fp8_scale_448_to_240", "amax / 448.0f", "amax / 240.0f", None),
     ("fwht_sign_f32", "v[i + h] = x - y;", "v[i + h] = y - x;", 0),
     ("fwht_sign_f64", "v[i + h] = x - y;", "v[i + h] = y - x;", 1),
-    ("fwht_missing_stage", "for (int h = 1; h < 32; h <<= 1) {", "for (int h = 1; h < 16; h <<= 1) {", None),
-    ("fwht_stage_order", "for (int h = 1; h < 32; h <<= 1) {\n    for (int i = 0; i < 32; ++i) {\n      if (i & h) continue;\n      float x",
-     "for (int hh = 16; hh >= 1; hh >>= 1) { int h = hh;\n    for (int i = 0; i < 32; ++i) {\n      if (i & h) continue;\n      float x", None),
+    ("fwht_missing_stage", "for (int h = 1; h < B; h <<= 1) {", "for (int h = 1; h < B / 2; h <<= 1) {", None),
+    ("fwht_stage_order", "for (int h = 1; h < B; h <<= 1) {\n    for (int i = 0; i < B; ++i) {\n      if (i & h) continue;\n      float x",
+     "for (int hh = B / 2; hh >= 1; hh >>= 1) { int h = hh;\n    for (int i = 0; i < B; ++i) {\n      if (i & h) continue;\n      float x", None),
+    ("fwht_order_only_above_32", "for (int h = 1; h < B; h <<= 1) {\n    for (int i = 0; i < B; ++i) {\n      if (i & h) continue;\n      float x",
+     "for (int hh = 1; hh < B; hh <<= 1) { int h = (B > 32 && hh >= 16) ? (hh == 16 ? B / 2 : hh / 2) : hh;\n    for (int i = 0; i < B; ++i) {\n      if (i & h) continue;\n      float x", None),
     ("h32_weights_not_divided", "r[j] = r[j] * 0.03125f;", "r[j] = r[j] * 0.0625f;", None),
+    ("rotated_weights_scale", "r[j] = r[j] * inv_b;", "r[j] = r[j] * (2.0f * inv_b);", None),
+    ("act_rotation_block_32", "const int B = hadamard == 1 ? 32 : hadamard;", "const int B = 32;", None),
     ("act_rotation_first_row_only", "  if (hadamard) {\n    for (int m = 0; m < M; ++m)",
      "  if (hadamard) {\n    for (int m = 0; m < 1; ++m)", None),
     ("product_drops_last_term", "          for (int64_t k = 0; k < K; ++k) {\n            double p = a[(int64_t)m * K + k] * w[k];",
