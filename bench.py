@@ -9,7 +9,8 @@ activation pre-pass and the verify kernel per call, chained with
 programmatic dependent launch) and timed with CUDA events on the launching
 stream.  value = compressed weight bytes streamed per step / step time.
 
-Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h,
+Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h
+(32-point rotation), q4_gateup_h128, q4_down_h128 (128-point rotation),
 fp8_mlp, model (64 layers x {qkv, out, gate+up, down}), q4_lmhead (the
 151,936 x 5120 output head through qmm_verify_greedy: the verify product plus
 the argmax and accepted-prefix step).
@@ -51,6 +52,9 @@ WORKLOADS = {
     "q4_gateup_h": ("q4_gateup", True, (16,)),
     "q4_down_h": ("q4_down", True, (16,)),
     "fp8_mlp": ("fp8_mlp", False, (1, 8, 16)),
+    # the 128-point rotation of the activations (weights rotated offline to match)
+    "q4_gateup_h128": ("q4_gateup", 128, (16,)),
+    "q4_down_h128": ("q4_down", 128, (16,)),
     # output head with the greedy acceptance step (qmm_verify_greedy)
     "q4_lmhead": ("q4_lmhead", False, (1, 8, 16)),
 }
@@ -289,7 +293,8 @@ def run_gpu(args, ws, rank, local):
             groups.append((M, items))
         per_copy_bytes = one
         fmt_name = "Q4_0" if spec["fmt"] == "q4_0" else "FP8 E4M3 128x128"
-        workload_desc = (f"{fmt_name} verify K={K} N={N}{' Hadamard32' if hadamard else ''}, "
+        rot = f" Hadamard{32 if hadamard is True else hadamard}" if hadamard else ""
+        workload_desc = (f"{fmt_name} verify K={K} N={N}{rot}, "
                          f"M={'/'.join(map(str, Ms))}, {copies} distinct weight copies "
                          f"({copies * one / 1e6:.0f} MB, > 4x L2) cycled")
         main_kernel = "verify_kernel<" + ("0" if spec["fmt"] == "q4_0" else "1")
@@ -320,7 +325,8 @@ def run_gpu(args, ws, rank, local):
     graphs = [(M, capture(torch, lambda it=items: run_group(it)), items) for M, items in groups]
     # kernels per call: the verify kernel, plus the activation pre-pass on the f16 paths
     calls_per_step = sum(len(items) for _, items in groups)
-    launches_per_step = sum(sum(1 + int(bool(m.info()["flags"] & q.QMM_FLAG_HADAMARD32)
+    rot_flags = q.QMM_FLAG_HADAMARD32 | q.QMM_FLAG_HADAMARD64 | q.QMM_FLAG_HADAMARD128
+    launches_per_step = sum(sum(1 + int(bool(m.info()["flags"] & rot_flags)
                                         or m.fmt == q.QMM_FMT_FP8_E4M3_B128)
                                 for m, _, _ in items) for _, items in groups)
     bytes_per_step = sum(sum(m.info()["weight_bytes"] for m, _, _ in items) for _, items in groups)

@@ -28,7 +28,11 @@
  * (strides 1,2,4,8,16, each stage (x, y) -> (x + y, x - y), fp32), for weights
  * that were rotated the same way offline and divided by 32 (see
  * qmm_quantize_q4_0), so the product equals the unrotated one
- * ["Qwen3.8-27B at 45.7 tok/s ...", same section].
+ * ["Qwen3.8-27B at 45.7 tok/s ...", same section].  QMM_FLAG_HADAMARD64 and
+ * QMM_FLAG_HADAMARD128 do the same with 64- and 128-point blocks, the larger
+ * rotations that page lists as its next step ("What's next"), with the same
+ * stride-ascending stage order (strides 1, 2, ..., B/2) and weights divided by
+ * B; at most one of the three is set.
  *
  * Conventions for every entry point:
  *   - Return value: QMM_OK (0) or one of the QMM_ERR_* codes below.  No call
@@ -80,7 +84,12 @@ enum {
    * tensor memory, one MMA issuer per CTA) instead of the default warp-level
    * mma.sync kernel.  Same results within the tolerance; slower at M <= 16,
    * where a 128x16x16 tcgen05 MMA costs about as much as a 128x256x16 one. */
-  QMM_FLAG_TCGEN05 = 1u << 2
+  QMM_FLAG_TCGEN05 = 1u << 2,
+  /* As QMM_FLAG_HADAMARD32 with 64- or 128-point blocks (weights rotated the
+   * same way offline and divided by 64 or 128); K must be a multiple of the
+   * block.  At most one rotation flag. */
+  QMM_FLAG_HADAMARD64 = 1u << 3,
+  QMM_FLAG_HADAMARD128 = 1u << 4
 };
 
 /* Description of one weight matrix W[N][K]. */
@@ -249,21 +258,31 @@ int qmm_dequantize(qmm_t h, float* w_out, void* stream);
 int qmm_hadamard32(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K,
                    void* stream);
 
+/* The same rotation with B-point blocks, B = block = 32, 64 or 128 (strides 1,
+ * 2, ..., B/2, each stage (x, y) -> (x + y, x - y), fp32).  K % B == 0.
+ * Errors: as qmm_hadamard32, plus INVALID_ARG for another block size.  Async. */
+int qmm_hadamard(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K, int block,
+                 void* stream);
+
 /* Quantize fp32 weights w (device [N][K]) into Q4_0 blocks (device, N*(K/32)*18
  * bytes, layout as in qmm_desc).  Per block: d32 = (element of largest
  * magnitude, first on ties, with its sign) / -8; q = clamp(roundf(w / d32) + 8,
  * 0, 15) using w * (1/d32); stored d = fp16 round-to-nearest-even of d32.
- * With QMM_FLAG_HADAMARD32 in flags every 32-block is first rotated with the
- * fp32 butterflies and divided by 32 (the offline half of the Hadamard
- * variant).  K % 32 == 0.  Async. */
+ * With QMM_FLAG_HADAMARD32 (64, 128) in flags every 32-block (64-, 128-block)
+ * is first rotated with the fp32 butterflies and divided by the block size
+ * (the offline half of the Hadamard variants).  K % 32 == 0 (and K a multiple
+ * of the rotation block).  The 64- and 128-point rotations go through a
+ * temporary fp32 copy of w allocated and freed in stream order on `stream`.
+ * Async. */
 int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
                       void* stream);
 
 /* Quantize fp32 weights w (device [N][K]) to E4M3 codes (device [N][K]) and
  * fp32 scales (device [N/128][K/128]): per 128x128 tile s = maxabs / 448 and
  * code = e4m3 round-to-nearest-even of w / s, saturated to +-448 (s == 0 gives
- * zero codes).  QMM_FLAG_HADAMARD32 rotates each 32-block first (and divides
- * by 32).  N % 128 == 0, K % 128 == 0.  Async. */
+ * zero codes).  QMM_FLAG_HADAMARD32 (64, 128) rotates each 32-block (64-,
+ * 128-block) first and divides by the block size, as qmm_quantize_q4_0.
+ * N % 128 == 0, K % 128 == 0.  Async. */
 int qmm_quantize_fp8(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* codes,
                      float* scales, void* stream);
 

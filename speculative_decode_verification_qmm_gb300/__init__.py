@@ -16,7 +16,7 @@ import ctypes
 
 from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_ARG,
                    QMM_ERR_M_RANGE, QMM_ERR_SHAPE, QMM_ERR_STATE, QMM_ERR_TIMEOUT,
-                   QMM_FLAG_HADAMARD32, QMM_FLAG_TCGEN05, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
+                   QMM_FLAG_HADAMARD32, QMM_FLAG_HADAMARD64, QMM_FLAG_HADAMARD128, QMM_FLAG_TCGEN05, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
@@ -28,7 +28,8 @@ __all__ = [
     "QMM_OK", "QMM_ERR_INVALID_ARG", "QMM_ERR_SHAPE", "QMM_ERR_M_RANGE", "QMM_ERR_ALIGN",
     "QMM_ERR_CUDA", "QMM_ERR_TIMEOUT", "QMM_ERR_STATE", "QMM_ERR_DEVICE",
     "QMM_FMT_Q4_0", "QMM_FMT_FP8_E4M3_B128", "QMM_FLAG_HADAMARD32", "QMM_FLAG_SIMT",
-    "QMM_FLAG_TCGEN05",
+    "QMM_FLAG_TCGEN05", "QMM_FLAG_HADAMARD64", "QMM_FLAG_HADAMARD128", "qmm_hadamard",
+    "rotation_flag", "hadamard",
 ]
 
 
@@ -144,6 +145,23 @@ def qmm_hadamard32(act, act_out, M: int, K: int, stream=None) -> None:
                                                    _stream_ptr(stream)))
 
 
+def qmm_hadamard(act, act_out, M: int, K: int, block: int, stream=None) -> None:
+    _check("qmm_hadamard", load().qmm_hadamard(_ptr(act), act.stride(0), _ptr(act_out), M, K,
+                                               block, _stream_ptr(stream)))
+
+
+def rotation_flag(hadamard) -> int:
+    """QMM_FLAG_HADAMARD* for hadamard = False, True (32), 32, 64 or 128."""
+    if hadamard is True:
+        return QMM_FLAG_HADAMARD32
+    if not hadamard:
+        return 0
+    flags = {32: QMM_FLAG_HADAMARD32, 64: QMM_FLAG_HADAMARD64, 128: QMM_FLAG_HADAMARD128}
+    if int(hadamard) not in flags:
+        raise ValueError(f"rotation block must be 32, 64 or 128, not {hadamard!r}")
+    return flags[int(hadamard)]
+
+
 def qmm_quantize_q4_0(w, blocks, flags: int = 0, stream=None) -> None:
     N, K = w.shape
     _check("qmm_quantize_q4_0", load().qmm_quantize_q4_0(_ptr(w), N, K, flags, _ptr(blocks),
@@ -165,23 +183,33 @@ def qmm_debug_fail_allocs(n: int) -> None:
 
 
 # ------------------------------------------------------------------ convenience
-def quantize_q4_0(w, hadamard: bool = False, stream=None):
-    """CUDA fp32 [N, K] -> CUDA uint8 [N, K/32, 18] Q4_0 blocks (device quantizer)."""
+def quantize_q4_0(w, hadamard=False, stream=None):
+    """CUDA fp32 [N, K] -> CUDA uint8 [N, K/32, 18] Q4_0 blocks (device quantizer);
+    hadamard = False, True (32), 32, 64 or 128 rotates the weights first."""
     import torch
     N, K = w.shape
     blocks = torch.empty((N, K // 32, 18), dtype=torch.uint8, device=w.device)
-    qmm_quantize_q4_0(w.contiguous(), blocks, QMM_FLAG_HADAMARD32 if hadamard else 0, stream)
+    qmm_quantize_q4_0(w.contiguous(), blocks, rotation_flag(hadamard), stream)
     return blocks
 
 
-def quantize_fp8(w, hadamard: bool = False, stream=None):
+def quantize_fp8(w, hadamard=False, stream=None):
     """CUDA fp32 [N, K] -> (uint8 codes [N, K], fp32 scales [N/128, K/128])."""
     import torch
     N, K = w.shape
     codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     scales = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
-    qmm_quantize_fp8(w.contiguous(), codes, scales, QMM_FLAG_HADAMARD32 if hadamard else 0, stream)
+    qmm_quantize_fp8(w.contiguous(), codes, scales, rotation_flag(hadamard), stream)
     return codes, scales
+
+
+def hadamard(act, block: int = 32, stream=None):
+    """CUDA bf16 [M, K] -> CUDA fp32 [M, K], every block-sized block rotated."""
+    import torch
+    M, K = act.shape
+    out = torch.empty((M, K), dtype=torch.float32, device=act.device)
+    qmm_hadamard(act, out, M, K, block, stream)
+    return out
 
 
 def hadamard32(act, stream=None):
@@ -196,9 +224,9 @@ def hadamard32(act, stream=None):
 class Matrix:
     """One weight matrix on the device, ready for repeated verify calls."""
 
-    def __init__(self, fmt: int, weights, N: int, K: int, scales=None, hadamard: bool = False,
+    def __init__(self, fmt: int, weights, N: int, K: int, scales=None, hadamard=False,
                  simt: bool = False, k_splits: int = 0, stream=None, tcgen05: bool = False):
-        flags = ((QMM_FLAG_HADAMARD32 if hadamard else 0) | (QMM_FLAG_SIMT if simt else 0)
+        flags = (rotation_flag(hadamard) | (QMM_FLAG_SIMT if simt else 0)
                  | (QMM_FLAG_TCGEN05 if tcgen05 else 0))
         self.N, self.K, self.fmt = N, K, fmt
         self.handle = qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream)

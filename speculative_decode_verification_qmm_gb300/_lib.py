@@ -25,6 +25,8 @@ QMM_FMT_FP8_E4M3_B128 = 1
 QMM_FLAG_HADAMARD32 = 1
 QMM_FLAG_SIMT = 2
 QMM_FLAG_TCGEN05 = 4
+QMM_FLAG_HADAMARD64 = 8
+QMM_FLAG_HADAMARD128 = 16
 
 
 class qmm_desc(ctypes.Structure):
@@ -81,6 +83,7 @@ SIGNATURES = {
     "qmm_strerror": (ctypes.c_char_p, [_INT]),
     "qmm_dequantize": (_INT, [_P, _P, _P]),
     "qmm_hadamard32": (_INT, [_P, _I64, _P, _INT, _I64, _P]),
+    "qmm_hadamard": (_INT, [_P, _I64, _P, _INT, _I64, _INT, _P]),
     "qmm_quantize_q4_0": (_INT, [_P, _I64, _I64, _U32, _P, _P]),
     "qmm_quantize_fp8": (_INT, [_P, _I64, _I64, _U32, _P, _P, _P]),
     "qmm_debug_set_wait_limit": (_INT, [_P, _I64]),

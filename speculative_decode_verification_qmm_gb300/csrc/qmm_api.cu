@@ -122,6 +122,19 @@ int cuda_fail(qmm_handle* h, cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+constexpr uint32_t ROTATION_FLAGS = QMM_FLAG_HADAMARD32 | QMM_FLAG_HADAMARD64 | QMM_FLAG_HADAMARD128;
+
+// Rotation block size of a flag set: 0 (none), 32, 64 or 128; -1 for more than one.
+int rotation_block(uint32_t flags) {
+  switch (flags & ROTATION_FLAGS) {
+    case 0: return 0;
+    case QMM_FLAG_HADAMARD32: return 32;
+    case QMM_FLAG_HADAMARD64: return 64;
+    case QMM_FLAG_HADAMARD128: return 128;
+    default: return -1;
+  }
+}
+
 // Choose the K split count S.  With S > 1 every CTA stays resident in one
 // wave (two CTAs per SM; tcgen05: as many clusters of S as the device holds at
 // once).  tcgen05: score = time to stream the padded bytes at min(HBM
@@ -335,19 +348,22 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   *out = nullptr;
   if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
   if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
-  if (d->flags & ~(uint32_t)(QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT | QMM_FLAG_TCGEN05))
+  if (d->flags & ~(uint32_t)(ROTATION_FLAGS | QMM_FLAG_SIMT | QMM_FLAG_TCGEN05))
     return QMM_ERR_INVALID_ARG;
+  const int rb = rotation_block(d->flags);
+  if (rb < 0) return QMM_ERR_INVALID_ARG;
   if (d->k_splits < 0) return QMM_ERR_INVALID_ARG;
   const int fmt = (int)d->format;
   if (fmt == 1 && !d->scales) return QMM_ERR_INVALID_ARG;
   if (fmt == 1 && (d->flags & QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
   // the tcgen05 kernel serves bf16 Q4_0 only: no rotation, not the CUDA-core baseline
   if ((d->flags & QMM_FLAG_TCGEN05) &&
-      (fmt != 0 || (d->flags & (QMM_FLAG_HADAMARD32 | QMM_FLAG_SIMT))))
+      (fmt != 0 || (d->flags & (ROTATION_FLAGS | QMM_FLAG_SIMT))))
     return QMM_ERR_INVALID_ARG;
   if (d->N < 1 || d->K < 1) return QMM_ERR_SHAPE;
   if (fmt == 0 && d->K % 32) return QMM_ERR_SHAPE;
   if (fmt == 1 && (d->N % 128 || d->K % 128)) return QMM_ERR_SHAPE;
+  if (rb > 0 && d->K % rb) return QMM_ERR_SHAPE;
   if (d->N > (1ll << 31) || d->K > (1ll << 31)) return QMM_ERR_SHAPE;
   int dev = 0, sms = 0;
   int rc = check_device(&dev, &sms);
@@ -485,7 +501,8 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
   cudaStream_t st = (cudaStream_t)stream;
   const Plan& p = h->plan;
-  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
+  const int hb = rotation_block(h->flags);
+  const bool had = hb > 0;
   const bool f16 = had || h->fmt == 1;
   // bf16 operands read the caller's rows directly; the f16 paths (Hadamard
   // rotation, FP8) go through the activation pre-pass and its scratch.
@@ -502,7 +519,7 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
     pp.S = p.S;
     pp.spc = p.spc;
     pp.stage_k = p.stage_k;
-    e = launch_act_prep(pp, f16, had, st);
+    e = launch_act_prep(pp, f16, hb, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
 
@@ -647,43 +664,87 @@ int qmm_dequantize(qmm_t h, float* w_out, void* stream) {
   return e == cudaSuccess ? QMM_OK : cuda_fail(h, e);
 }
 
-int qmm_hadamard32(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K, void* stream) {
+int qmm_hadamard(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K, int block,
+                 void* stream) {
   if (!act || !act_out) return QMM_ERR_INVALID_ARG;
+  if (block != 32 && block != 64 && block != 128) return QMM_ERR_INVALID_ARG;
   if (M < 1) return QMM_ERR_M_RANGE;
-  if (K < 32 || K % 32) return QMM_ERR_SHAPE;
+  if (K < block || K % block) return QMM_ERR_SHAPE;
   if (((uintptr_t)act & 15) || ((uintptr_t)act_out & 15) || lda < K || (lda & 7)) return QMM_ERR_ALIGN;
   int dev = 0, sms = 0;
   int rc = check_device(&dev, &sms);
   if (rc != QMM_OK) return rc;
-  cudaError_t e = launch_hadamard32(act, lda, act_out, M, K, sms, (cudaStream_t)stream);
+  cudaError_t e = launch_hadamard(act, lda, act_out, M, K, block, sms, (cudaStream_t)stream);
   return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
 }
+
+int qmm_hadamard32(const uint16_t* act, int64_t lda, float* act_out, int M, int64_t K, void* stream) {
+  return qmm_hadamard(act, lda, act_out, M, K, 32, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The weights w rotated in rb-blocks (64 or 128) and divided by rb, in a
+// temporary buffer allocated and freed in stream order; the plain quantizer
+// `quant` then reads it.
+template <typename F>
+cudaError_t quantize_rotated(const float* w, int64_t N, int64_t K, int rb, cudaStream_t st, F quant) {
+  void* tmp = nullptr;
+  cudaError_t e = cudaMallocAsync(&tmp, (size_t)N * (size_t)K * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  e = launch_rotate_weights(w, N, K, rb, reinterpret_cast<float*>(tmp), st);
+  if (e == cudaSuccess) e = quant(reinterpret_cast<const float*>(tmp));
+  const cudaError_t f = cudaFreeAsync(tmp, st);
+  return e != cudaSuccess ? e : f;
+}
+
+}  // namespace
+
+extern "C" {
 
 int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
                       void* stream) {
   if (!w || !blocks) return QMM_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)QMM_FLAG_HADAMARD32) return QMM_ERR_INVALID_ARG;
-  if (N < 1 || K < 32 || K % 32) return QMM_ERR_SHAPE;
+  if (flags & ~ROTATION_FLAGS) return QMM_ERR_INVALID_ARG;
+  const int rb = rotation_block(flags);
+  if (rb < 0) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32 || (rb > 0 && K % rb)) return QMM_ERR_SHAPE;
   if ((uintptr_t)w & 15) return QMM_ERR_ALIGN;
   int dev = 0, sms = 0;
   int rc = check_device(&dev, &sms);
   if (rc != QMM_OK) return rc;
-  cudaError_t e = launch_quantize_q4(w, N, K, (flags & QMM_FLAG_HADAMARD32) ? 1 : 0, blocks,
-                                     (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+  if (rb > 32)
+    e = quantize_rotated(w, N, K, rb, st, [&](const float* r) {
+      return launch_quantize_q4(r, N, K, 0, blocks, st);
+    });
+  else
+    e = launch_quantize_q4(w, N, K, rb == 32 ? 1 : 0, blocks, st);
   return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
 }
 
 int qmm_quantize_fp8(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* codes,
                      float* scales, void* stream) {
   if (!w || !codes || !scales) return QMM_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)QMM_FLAG_HADAMARD32) return QMM_ERR_INVALID_ARG;
+  if (flags & ~ROTATION_FLAGS) return QMM_ERR_INVALID_ARG;
+  const int rb = rotation_block(flags);
+  if (rb < 0) return QMM_ERR_INVALID_ARG;
   if (N < 128 || K < 128 || N % 128 || K % 128) return QMM_ERR_SHAPE;
   if (((uintptr_t)w & 15) || ((uintptr_t)codes & 15)) return QMM_ERR_ALIGN;
   int dev = 0, sms = 0;
   int rc = check_device(&dev, &sms);
   if (rc != QMM_OK) return rc;
-  cudaError_t e = launch_quantize_fp8(w, N, K, (flags & QMM_FLAG_HADAMARD32) ? 1 : 0, codes, scales,
-                                      (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+  if (rb > 32)
+    e = quantize_rotated(w, N, K, rb, st, [&](const float* r) {
+      return launch_quantize_fp8(r, N, K, 0, codes, scales, st);
+    });
+  else
+    e = launch_quantize_fp8(w, N, K, rb == 32 ? 1 : 0, codes, scales, st);
   return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
 }
 
@@ -740,7 +801,8 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
   const Plan& p = h->plan;
-  const bool had = (h->flags & QMM_FLAG_HADAMARD32) != 0;
+  const int hb = rotation_block(h->flags);
+  const bool had = hb > 0;
   const bool f16 = had || h->fmt == 1;
   // Carve the array: activation scratch | per-(row, split) factors.  Both are
   // written in full by the pre-pass before the verify kernel reads them, so
@@ -766,7 +828,7 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
     pp.S = p.S;
     pp.spc = p.spc;
     pp.stage_k = p.stage_k;
-    e = launch_act_prep(pp, f16, had, st);
+    e = launch_act_prep(pp, f16, hb, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
 

@@ -9,17 +9,21 @@
 namespace qmm {
 
 // ---------------------------------------------------------------------------
-// 32-point Walsh-Hadamard rotation across 8 lanes holding 4 consecutive values
-// each: strides 1 and 2 inside the lane, then strides 4, 8 and 16 with lane
-// shuffles (partner lane = lane ^ 1, ^ 2, ^ 4).  Every stage maps the pair
-// (x at the lower index, y at the upper) to (x + y, x - y) in fp32, which is
-// the stage order and arithmetic of the unnormalised transform
-// ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve, and 4-bit activations
-// with a Hadamard rotation", section "Prompt processing: 4-bit activations,
-// rotated first": two in-register butterfly steps and three lane shuffles].
-// All 32 lanes of the warp must call it (groups of 8 lanes = 4 blocks).
+// B-point Walsh-Hadamard rotation (B = 32, 64 or 128) across B/4 lanes holding
+// 4 consecutive values each: strides 1 and 2 inside the lane, then strides
+// 4, 8, ..., B/2 with lane shuffles (partner lane = lane ^ 1, ^ 2, ..., ^ B/8).
+// Every stage maps the pair (x at the lower index, y at the upper) to
+// (x + y, x - y) in fp32, the stage order and arithmetic of the unnormalised
+// transform ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve, and 4-bit
+// activations with a Hadamard rotation", section "Prompt processing: 4-bit
+// activations, rotated first": two in-register butterfly steps and three lane
+// shuffles for B = 32; the larger rotations that the page names as the next
+// step keep the stride-ascending order].  All 32 lanes of the warp must call
+// it (a warp holds 128 values: 128 / B blocks).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void fwht32_lanes(float (&v)[4], int lane) {
+template <int B>
+__device__ __forceinline__ void fwht_lanes(float (&v)[4], int lane) {
+  static_assert(B == 32 || B == 64 || B == 128, "rotation size");
   float x, y;
   // stride 1: (0,1), (2,3)
   x = v[0]; y = v[1]; v[0] = __fadd_rn(x, y); v[1] = __fsub_rn(x, y);
@@ -27,9 +31,9 @@ __device__ __forceinline__ void fwht32_lanes(float (&v)[4], int lane) {
   // stride 2: (0,2), (1,3)
   x = v[0]; y = v[2]; v[0] = __fadd_rn(x, y); v[2] = __fsub_rn(x, y);
   x = v[1]; y = v[3]; v[1] = __fadd_rn(x, y); v[3] = __fsub_rn(x, y);
-  // strides 4, 8, 16 across lanes
+  // strides 4 .. B/2 across lanes
 #pragma unroll
-  for (int d = 1; d <= 4; d <<= 1) {
+  for (int d = 1; d < B / 4; d <<= 1) {
     const bool upper = (lane & d) != 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -51,14 +55,15 @@ __device__ __forceinline__ void load4_bf16(const uint16_t* p, float (&v)[4]) {
 // Activation pre-pass.  CTA (s, m) converts row m's K range of split s into the
 // stage-ordered 16-bit scratch read by the verify kernel.
 //   OUT_F16 = false: bf16 copied unchanged (exact); multiplier 1.
-//   OUT_F16 = true : values (rotated when HAD) are multiplied by 2^e with e
+//   OUT_F16 = true : values (rotated in HB-blocks when HB != 0) are multiplied by 2^e with e
 //                    chosen so that the largest magnitude of the range lands
 //                    in [2^14, 2^15), rounded to f16, and 2^-e is recorded as
 //                    the multiplier of this (row, split)'s partial sums.
 // Elements past K are written as zeros.
 // ---------------------------------------------------------------------------
-template <bool OUT_F16, bool HAD>
+template <bool OUT_F16, int HB>
 __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ PrepParams p) {
+  constexpr bool HAD = HB != 0;
   pdl_trigger();
   const int s = blockIdx.x, m = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -89,7 +94,7 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
       const int64_t k = k0 + kl;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (k < p.K) load4_bf16(src + k, v);
-      if constexpr (HAD) fwht32_lanes(v, lane);
+      if constexpr (HAD) fwht_lanes<HB>(v, lane);
 #pragma unroll
       for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[e]));
     }
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
       const int64_t k = k0 + kl;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (k < p.K) load4_bf16(src + k, v);
-      if constexpr (HAD) fwht32_lanes(v, lane);
+      if constexpr (HAD) fwht_lanes<HB>(v, lane);
       const __half2 h01 = __floats2half2_rn(v[0] * mul, v[1] * mul);
       const __half2 h23 = __floats2half2_rn(v[2] * mul, v[3] * mul);
       uint2 o;
@@ -129,9 +134,10 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
   }
 }
 
-// Standalone rotation: fp32 output [M][K], each warp rotates 4 blocks at a time.
-__global__ void __launch_bounds__(256) hadamard32_kernel(const uint16_t* __restrict__ act, int64_t lda,
-                                                         float* __restrict__ out, int M, int64_t K) {
+// Standalone rotation: fp32 output [M][K], each warp rotates 128 / HB blocks at a time.
+template <int HB>
+__global__ void __launch_bounds__(256) hadamard_kernel(const uint16_t* __restrict__ act, int64_t lda,
+                                                       float* __restrict__ out, int M, int64_t K) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   const int64_t per_row = K / 128 + ((K % 128) ? 1 : 0);  // 128-element groups per row
@@ -139,9 +145,9 @@ __global__ void __launch_bounds__(256) hadamard32_kernel(const uint16_t* __restr
     const int m = (int)(wid / per_row);
     const int64_t k = (wid % per_row) * 128 + lane * 4;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool ok = k < K;  // K % 32 == 0: an 8-lane group is all in or all out
+    const bool ok = k < K;  // K % HB == 0: a block's lanes are all in or all out
     if (ok) load4_bf16(act + (int64_t)m * lda + k, v);
-    fwht32_lanes(v, lane);
+    fwht_lanes<HB>(v, lane);
     if (ok) *reinterpret_cast<float4*>(out + (int64_t)m * K + k) = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
@@ -335,6 +341,33 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, const float
 // ---------------------------------------------------------------------------
 // Quantizers (offline tools).
 // ---------------------------------------------------------------------------
+// The offline weight rotation of the 64- and 128-point variants, ahead of the
+// plain quantizers: every HB-block of a row of w [N][K] fp32 rotated with
+// fwht_lanes and multiplied by 1/HB (a power of two, exact) into out.
+template <int HB>
+__global__ void __launch_bounds__(256) rotate_weights_kernel(const float* __restrict__ w, int64_t N,
+                                                             int64_t K, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  const int64_t per_row = K / 128 + ((K % 128) ? 1 : 0);
+  for (int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); wid < per_row * N; wid += warps) {
+    const int64_t n = wid / per_row;
+    const int64_t k = (wid % per_row) * 128 + lane * 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool ok = k < K;  // K % HB == 0: a block's lanes are all in or all out
+    if (ok) {
+      const float4 f = *reinterpret_cast<const float4*>(w + n * K + k);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    }
+    fwht_lanes<HB>(v, lane);
+    constexpr float inv = 1.0f / (float)HB;
+    if (ok)
+      *reinterpret_cast<float4*>(out + n * K + k) =
+          make_float4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
+                      __fmul_rn(v[3], inv));
+  }
+}
+
 // Rotate a 32-block held by one thread (same stage order as fwht32_lanes).
 __device__ __forceinline__ void fwht32_thread(float (&v)[32]) {
 #pragma unroll
@@ -478,7 +511,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const float* __restri
 // ---------------------------------------------------------------------------
 // Host launchers.
 // ---------------------------------------------------------------------------
-cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStream_t st) {
+cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, int hb, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.M, 1);
   cfg.blockDim = dim3(256, 1, 1);
@@ -489,19 +522,42 @@ cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!out_f16) return cudaLaunchKernelEx(&cfg, act_prep_kernel<false, false>, p);
-  if (had) return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, true>, p);
-  return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, false>, p);
+  if (!out_f16) return cudaLaunchKernelEx(&cfg, act_prep_kernel<false, 0>, p);
+  switch (hb) {
+    case 32: return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, 32>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, 64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, 128>, p);
+    default: return cudaLaunchKernelEx(&cfg, act_prep_kernel<true, 0>, p);
+  }
 }
 
-cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int M, int64_t K,
-                              int sm_count, cudaStream_t st) {
+cudaError_t launch_hadamard(const uint16_t* act, int64_t lda, float* out, int M, int64_t K, int hb,
+                            int sm_count, cudaStream_t st) {
   const int64_t work = (K / 128 + 1) * M;
   int64_t blocks = (work + 7) / 8;
   const int64_t cap = (int64_t)sm_count * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  hadamard32_kernel<<<(unsigned)blocks, 256, 0, st>>>(act, lda, out, M, K);
+  if (hb == 128)
+    hadamard_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(act, lda, out, M, K);
+  else if (hb == 64)
+    hadamard_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(act, lda, out, M, K);
+  else
+    hadamard_kernel<32><<<(unsigned)blocks, 256, 0, st>>>(act, lda, out, M, K);
+  return cudaGetLastError();
+}
+
+// w rotated in hb-blocks (hb = 64 or 128) and times 1/hb into out (fp32 [N][K]).
+cudaError_t launch_rotate_weights(const float* w, int64_t N, int64_t K, int hb, float* out,
+                                  cudaStream_t st) {
+  const int64_t work = (K / 128 + 1) * N;
+  int64_t blocks = (work + 7) / 8;
+  if (blocks > 65535ll * 8) blocks = 65535ll * 8;
+  if (blocks < 1) blocks = 1;
+  if (hb == 128)
+    rotate_weights_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, out);
+  else
+    rotate_weights_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, out);
   return cudaGetLastError();
 }
 

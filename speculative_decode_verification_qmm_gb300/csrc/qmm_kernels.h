@@ -45,10 +45,15 @@ cudaError_t launch_dequant_tc(const uint8_t* wdev, int64_t N, int64_t K, int n_t
 cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
 cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
 
-cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, bool had, cudaStream_t st);
-cudaError_t launch_hadamard32(const uint16_t* act, int64_t lda, float* out, int M, int64_t K,
-                              int sm_count, cudaStream_t st);
-// FP8: f8_scale receives [n_tiles][S * spc] tile scales (zero past N or K).
+// The activation pre-pass of the f16 operand paths; hb = rotation block size
+// (0 none, 32, 64, 128).
+cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, int hb, cudaStream_t st);
+// Rotation of activation rows in hb-blocks (32, 64, 128) to fp32.
+cudaError_t launch_hadamard(const uint16_t* act, int64_t lda, float* out, int M, int64_t K, int hb,
+                            int sm_count, cudaStream_t st);
+// Offline weight rotation in hb-blocks (64, 128), times 1/hb.
+cudaError_t launch_rotate_weights(const float* w, int64_t N, int64_t K, int hb, float* out,
+                                  cudaStream_t st);
 cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
                           int n_tiles, int S, int spc, uint8_t* wdev, float* f8_scale,
                           cudaStream_t st);

@@ -126,6 +126,19 @@ def test_host_validation_without_device(L):
     assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
     d.flags = q.QMM_FLAG_TCGEN05 | q.QMM_FLAG_SIMT
     assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    # at most one rotation; the rotation block divides K; none with tcgen05
+    d.flags = q.QMM_FLAG_HADAMARD32 | q.QMM_FLAG_HADAMARD64
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_TCGEN05 | q.QMM_FLAG_HADAMARD128
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_HADAMARD64
+    d.K = 96
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_SHAPE
+    d.flags = q.QMM_FLAG_HADAMARD128
+    d.K = 192
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_SHAPE
+    d.K = 32
+    d.flags = 0
     assert h.value is None
     # tool entry points validate shapes first
     assert L.qmm_quantize_q4_0(None, 4, 32, 0, None, None) == q.QMM_ERR_INVALID_ARG
@@ -133,6 +146,13 @@ def test_host_validation_without_device(L):
     assert L.qmm_quantize_fp8(w.ctypes.data, 100, 128, 0, w.ctypes.data, s.ctypes.data, None) == q.QMM_ERR_SHAPE
     assert L.qmm_hadamard32(w.ctypes.data, 64, w.ctypes.data, 0, 64, None) == q.QMM_ERR_M_RANGE
     assert L.qmm_hadamard32(w.ctypes.data, 64, w.ctypes.data, 1, 40, None) == q.QMM_ERR_SHAPE
+    assert L.qmm_hadamard(w.ctypes.data, 64, w.ctypes.data, 1, 64, 48, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_hadamard(w.ctypes.data, 96, w.ctypes.data, 1, 96, 64, None) == q.QMM_ERR_SHAPE
+    assert L.qmm_hadamard(w.ctypes.data, 64, w.ctypes.data, 0, 64, 64, None) == q.QMM_ERR_M_RANGE
+    H32_64 = q.QMM_FLAG_HADAMARD32 | q.QMM_FLAG_HADAMARD64
+    assert L.qmm_quantize_q4_0(w.ctypes.data, 4, 64, H32_64, w.ctypes.data, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize_q4_0(w.ctypes.data, 4, 64, q.QMM_FLAG_HADAMARD128, w.ctypes.data, None) == q.QMM_ERR_SHAPE
+    assert L.qmm_quantize_fp8(w.ctypes.data, 128, 128, q.QMM_FLAG_SIMT, w.ctypes.data, s.ctypes.data, None) == q.QMM_ERR_INVALID_ARG
 
 
 # ---------------------------------------------------------------- input generators
