@@ -20,6 +20,8 @@ Pin status (what fixes each function other than itself; see tests/test_oracle_pi
                                   half-size recursion that fixes the stage order
   verify product               -- M independent GEMVs, brute force vs numpy and exact
                                   rationals, one-hot and all-ones special cases
+  Q8_0 quantize / dequant      -- closed form, hand blocks (tests/golden/q8_0_blocks.json),
+                                  exhaustive codes x scales, quantizer bounds and ties
   greedy acceptance            -- hand-worked cases (tests/golden/greedy_accept.json),
                                   numpy's first-occurrence argmax, brute-force prefix
 """
@@ -37,11 +39,13 @@ __all__ = [
     "fwht32_f32", "fwht32_f64", "hadamard32_act_f32", "q4_0_quantize", "q4_0_quantize_h32",
     "fwht_f32", "fwht_f64", "hadamard_act_f32", "rotate_weights_f32",
     "q4_0_dequant", "fp8_quantize", "fp8_dequant", "matmul_f64", "verify_rows",
-    "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8", "greedy_accept",
+    "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8", "FMT_Q8_0", "greedy_accept",
+    "q8_0_quantize", "q8_0_dequant",
 ]
 
 FMT_Q4_0 = 0
 FMT_FP8 = 1
+FMT_Q8_0 = 2
 
 _lib = None
 
@@ -66,6 +70,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_fwht_f64.argtypes = [_P, _P, _INT]
     L.oracle_hadamard_act_f32.argtypes = [_P, _I64, _INT, _I64, _INT, _P]
     L.oracle_rotate_weights_f32.argtypes = [_P, _I64, _I64, _INT, _P]
+    L.oracle_q8_0_quantize.argtypes = [_P, _I64, _I64, _P]
+    L.oracle_q8_0_dequant.argtypes = [_P, _I64, _I64, _P]
     L.oracle_greedy_accept.restype = _INT
     L.oracle_greedy_accept.argtypes = [_P, _I64, _INT, _I64, _P, _P, _P]
     L.oracle_fwht32_f32.argtypes = [_P, _P]
@@ -247,6 +253,23 @@ def q4_0_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- FP8
+def q8_0_quantize(w: np.ndarray) -> np.ndarray:
+    """[N][K] fp32 -> canonical Q8_0 bytes, shape [N][K/32][34] uint8."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    out = np.empty((N, K // 32, 34), np.uint8)
+    lib().oracle_q8_0_quantize(_ptr(w), N, K, _ptr(out))
+    return out
+
+
+def q8_0_dequant(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    b = _c(blocks, np.uint8)
+    out = np.empty((N, K), np.float64)
+    lib().oracle_q8_0_dequant(_ptr(b), N, K, _ptr(out))
+    return out
+
+
 def fp8_quantize(w: np.ndarray):
     """[N][K] fp32 -> (codes [N][K] uint8, scales [ceil(N/128)][ceil(K/128)] fp32)."""
     w = _c(w, np.float32)

@@ -317,6 +317,60 @@ void oracle_q4_0_dequant(const uint8_t* blocks, int64_t N, int64_t K, double* w)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Q8_0: 32-element blocks, fp16 scale, 8-bit signed codes.                   */
+/* ------------------------------------------------------------------------ */
+/* The pages name Q8_0 as a reference format beside Q4_0 ["Qwen3.8-27B on the
+ * AMD R9700: up to 227 tok/s", TL;DR] and do not define it; the reading here
+ * is the GGUF layout of the same family as Q4_0: per 32 consecutive elements
+ * of a row, an fp16 scale d (little endian) then 32 two's-complement int8
+ * codes q, and w = d * q.  Quantizer: amax = largest |x| of the block,
+ * d32 = amax / 127, inv = 1/d32 (0 for an all-zero block),
+ * q = clamp(roundf(x * inv), -127, 127) (round half away from zero), stored
+ * d = fp16_rne(d32). */
+static void q8_0_quantize_block(const float* x, uint8_t* blk) {
+  float amax = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    float ax = fabsf(x[j]);
+    if (ax > amax) amax = ax;
+  }
+  float d32 = amax / 127.0f;
+  float inv = (d32 != 0.0f) ? 1.0f / d32 : 0.0f;
+  uint16_t d16 = oracle_f32_to_f16_rne(d32);
+  blk[0] = (uint8_t)(d16 & 0xFF);
+  blk[1] = (uint8_t)(d16 >> 8);
+  for (int j = 0; j < 32; ++j) {
+    int qi = (int)roundf(x[j] * inv);
+    if (qi < -127) qi = -127;
+    if (qi > 127) qi = 127;
+    blk[2 + j] = (uint8_t)(int8_t)qi;
+  }
+}
+
+/* w: [N][K] fp32 row-major; blocks: N * (K/32) * 34 bytes, row-major over n. */
+void oracle_q8_0_quantize(const float* w, int64_t N, int64_t K, uint8_t* blocks) {
+  int64_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b)
+      q8_0_quantize_block(w + n * K + 32 * b, blocks + (n * nb + b) * 34);
+}
+
+/* Dequantize one weight row to fp64: w = d * q. */
+static void q8_0_dequant_row(const uint8_t* blocks, int64_t n, int64_t K, double* row) {
+  int64_t nb = K / 32;
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t* blk = blocks + (n * nb + b) * 34;
+    double d = oracle_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+    for (int j = 0; j < 32; ++j) row[32 * b + j] = d * (double)(int8_t)blk[2 + j];
+  }
+}
+
+void oracle_q8_0_dequant(const uint8_t* blocks, int64_t N, int64_t K, double* w) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) q8_0_dequant_row(blocks, n, K, w + n * K);
+}
+
+/* ------------------------------------------------------------------------ */
 /* FP8 E4M3 with 128x128 fp32 scales.                                        */
 /* ------------------------------------------------------------------------ */
 
@@ -404,14 +458,15 @@ static void decode_act(const uint16_t* act, int64_t lda, int M, int64_t K, int h
 
 /* Verify product for a selection of weight rows, dequantizing row by row so
  * that full-size matrices need no [N][K] fp64 buffer.
- *   fmt: 0 = Q4_0 (wbytes = blocks), 1 = FP8 (wbytes = codes, scales)
+ *   fmt: 0 = Q4_0 (wbytes = blocks), 1 = FP8 (wbytes = codes, scales),
+ *        2 = Q8_0 (wbytes = blocks)
  *   rows: nrows output-feature indices (NULL = all N, nrows ignored)
  *   out, S: [M][nrows] fp64 (S may be NULL) */
 int oracle_verify_rows(int fmt, const uint8_t* wbytes, const float* scales, int64_t N,
                        int64_t K, const uint16_t* act, int64_t lda, int M, int hadamard,
                        const int64_t* rows, int64_t nrows, double* out, double* S) {
   const int hb = hadamard == 1 ? 32 : hadamard;
-  if (K <= 0 || N <= 0 || M <= 0 || (fmt == 0 && K % 32) ||
+  if (K <= 0 || N <= 0 || M <= 0 || fmt < 0 || fmt > 2 || ((fmt == 0 || fmt == 2) && K % 32) ||
       (hb && ((hb != 32 && hb != 64 && hb != 128) || K % hb)))
     return -1;
   if (!rows) nrows = N;
@@ -431,6 +486,8 @@ int oracle_verify_rows(int fmt, const uint8_t* wbytes, const float* scales, int6
         int64_t n = rows ? rows[i] : i;
         if (fmt == 0)
           q4_0_dequant_row(wbytes, n, K, w);
+        else if (fmt == 2)
+          q8_0_dequant_row(wbytes, n, K, w);
         else
           fp8_dequant_row(wbytes, scales, n, K, w);
         for (int m = 0; m < M; ++m) {

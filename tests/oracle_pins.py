@@ -444,6 +444,77 @@ def check_hadamard_act_model(O):
             assert (np.abs(got[m, 32 * b:32 * b + 32] - ref) <= bound).all()
 
 
+# ---------------------------------------------------------------- Q8_0
+def check_q8_0_dequant_closed_form(O):
+    """Hand-worked blocks (tests/golden/q8_0_blocks.json), then every code
+    under a few scales: w = d * (signed code)."""
+    for blk in _golden("q8_0_blocks.json")["blocks"]:
+        b = np.array(blk["bytes"], np.uint8).reshape(1, 1, 34)
+        got = O.q8_0_dequant(b, 1, 32)[0]
+        assert (got == np.array(blk["values"], np.float64)).all(), blk["name"]
+    codes = np.arange(256, dtype=np.uint8)
+    for d_bits in (0x3C00, 0x3800, 0xB400, 0x0001, 0x7BFF, 0x0000):
+        d = float(np.array([d_bits], np.uint16).view(np.float16)[0])
+        b = np.zeros((1, 8, 34), np.uint8)
+        b[0, :, 0], b[0, :, 1] = d_bits & 0xFF, d_bits >> 8
+        b[0, :, 2:] = codes.reshape(8, 32)
+        got = O.q8_0_dequant(b, 1, 256)[0]
+        assert (got == d * codes.view(np.int8).astype(np.float64)).all(), hex(d_bits)
+
+
+def check_q8_0_quantizer(O):
+    """Bounds and rules of the quantizer: the largest magnitude maps to +-127,
+    every element is within |d| / 2 of its dequantized value (plus the fp16
+    rounding of d times 127), signs survive, an all-zero block has d = 0 and
+    zero codes, and halves round away from zero (checked on a block whose
+    scale is exactly 1)."""
+    import speculative_decode_verification_qmm_gb300.synth as synth
+    w = synth.weights(64, 256, 31)
+    w[0, :32] = 0.0
+    b = O.q8_0_quantize(w)
+    deq = O.q8_0_dequant(b, 64, 256)
+    codes = b[:, :, 2:].view(np.int8).astype(np.int64)
+    d = b[:, :, :2].copy().view(np.uint16)[..., 0].view(np.float16).astype(np.float64)
+    x = w.reshape(64, 8, 32).astype(np.float64)
+    amax = np.abs(x).max(axis=2)
+    nz = amax > 0
+    top = np.abs(codes)[np.arange(64)[:, None], np.arange(8)[None, :], np.abs(x).argmax(axis=2)]
+    assert (top[nz] == 127).all()
+    d32 = amax / 127.0
+    # the stored scale is amax / 127 rounded to fp16: within half an fp16 ulp
+    # (2^-11 relative for normals, 2^-25 absolute for subnormals)
+    dq = 2.0 ** -11 * d32 + 2.0 ** -25
+    assert (np.abs(d - d32) <= dq * (1 + 1e-6)).all()
+    err = np.abs(x - deq.reshape(64, 8, 32))
+    bound = d32[..., None] / 2 + dq[..., None] * 127
+    assert (err <= bound * (1 + 1e-6)).all()
+    assert ((np.sign(codes) == np.sign(x)) | (codes == 0)).all()
+    assert (codes[~nz] == 0).all() and (d[~nz] == 0).all()
+    # scale exactly 1: amax 127; 2.5 -> 3, -2.5 -> -3, 0.5 -> 1, -0.5 -> -1
+    t = np.zeros((1, 32), np.float32)
+    t[0, :5] = [127.0, 2.5, -2.5, 0.5, -0.5]
+    c = O.q8_0_quantize(t)[0, 0, 2:7].view(np.int8).tolist()
+    assert c == [127, 3, -3, 1, -1], c
+
+
+def check_q8_0_product(O):
+    """The Q8_0 verify product against numpy's matmul of the dequantized
+    weights and against exact rationals on a small case."""
+    import speculative_decode_verification_qmm_gb300.synth as synth
+    N, K, M = 24, 96, 4
+    w = synth.weights(N, K, 33)
+    b = O.q8_0_quantize(w)
+    a = synth.activations(M, K, 34, outliers=True)
+    out, S = O.verify_rows(O.FMT_Q8_0, b, None, N, K, a)
+    af = synth.bf16_bits_to_f32(a).astype(np.float64)
+    deq = O.q8_0_dequant(b, N, K)
+    ref = af @ deq.T
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.allclose(S, np.abs(af) @ np.abs(deq).T, rtol=1e-12)
+    exact = sum(Fraction(float(af[1, k])) * Fraction(float(deq[5, k])) for k in range(K))
+    assert abs(Fraction(float(out[1, 5])) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 60)
+
+
 # ---------------------------------------------------------------- greedy acceptance
 def check_greedy_golden(O):
     """Hand-worked blocks (tests/golden/greedy_accept.json)."""
@@ -484,5 +555,6 @@ ALL_CHECKS = [
     check_q4_0_quantizer, check_fp8_quantizer, check_hadamard, check_rotated_product,
     check_product_brute_force, check_rows_are_independent_gemvs, check_special_activations,
     check_hadamard_act_model, check_greedy_golden, check_greedy_vs_library,
-    check_hadamard_larger, check_rotated_product_larger,
+    check_hadamard_larger, check_rotated_product_larger, check_q8_0_dequant_closed_form,
+    check_q8_0_quantizer, check_q8_0_product,
 ]

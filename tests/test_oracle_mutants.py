@@ -53,6 +53,11 @@ MUTANTS = [
     ("product_sabs_signed", "            sabs += fabs(p);\n          }\n          out[(int64_t)m * nrows + i]",
      "            sabs += p;\n          }\n          out[(int64_t)m * nrows + i]", None),
     ("product_wrong_act_row", "double p = a[(int64_t)m * K + k] * w[k];", "double p = a[(int64_t)(M - 1 - m) * K + k] * w[k];", None),
+    ("q8_codes_unsigned", "d * (double)(int8_t)blk[2 + j]", "d * (double)blk[2 + j]", None),
+    ("q8_scale_128", "float d32 = amax / 127.0f;", "float d32 = amax / 128.0f;", None),
+    ("q8_round_trunc", "int qi = (int)roundf(x[j] * inv);", "int qi = (int)(x[j] * inv);", None),
+    ("q8_drops_sign_of_d", "(uint16_t)(blk[0] | (blk[1] << 8)));\n    for (int j = 0; j < 32; ++j) row",
+     "(uint16_t)(blk[0] | ((blk[1] & 0x7F) << 8)));\n    for (int j = 0; j < 32; ++j) row", None),
     ("greedy_last_tie", "if (row[n] > row[best]) best = n;", "if (row[n] >= row[best]) best = n;", None),
     ("greedy_argmin", "if (row[n] > row[best]) best = n;", "if (row[n] < row[best]) best = n;", None),
     ("greedy_token_offset", "argmax[k] == tokens[k + 1]", "argmax[k] == tokens[k]", None),
