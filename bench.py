@@ -11,6 +11,7 @@ stream.  value = compressed weight bytes streamed per step / step time.
 
 Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h
 (32-point rotation), q4_gateup_h128, q4_down_h128 (128-point rotation),
+q8_mlp, q8_attn (Q8_0 at the FP8 MLP and the attention shapes),
 fp8_mlp, model (64 layers x {qkv, out, gate+up, down}), q4_lmhead (the
 151,936 x 5120 output head through qmm_verify_greedy: the verify product plus
 the argmax and accepted-prefix step).
@@ -55,6 +56,9 @@ WORKLOADS = {
     # the 128-point rotation of the activations (weights rotated offline to match)
     "q4_gateup_h128": ("q4_gateup", 128, (16,)),
     "q4_down_h128": ("q4_down", 128, (16,)),
+    # Q8_0 (fp16 scale per 32 elements, int8 codes)
+    "q8_mlp": ("q8_mlp", False, (1, 8, 16)),
+    "q8_attn": ("q8_attn", False, (1, 8, 16)),
     # output head with the greedy acceptance step (qmm_verify_greedy)
     "q4_lmhead": ("q4_lmhead", False, (1, 8, 16)),
 }
@@ -209,6 +213,11 @@ def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, s
             mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=hadamard, k_splits=splits,
                                  **kf))
             del blocks
+        elif spec["fmt"] == "q8_0":
+            blocks = q.quantize_q8_0(w, hadamard=hadamard)
+            del w
+            mats.append(q.Matrix(q.QMM_FMT_Q8_0, blocks, N, K, hadamard=hadamard, k_splits=splits))
+            del blocks
         else:
             codes, scales = q.quantize_fp8(w, hadamard=hadamard)
             del w
@@ -282,7 +291,8 @@ def run_gpu(args, ws, rank, local):
         shape_name, hadamard, Ms = WORKLOADS[args.workload]
         spec = synth.SHAPES[shape_name]
         N, K = spec["N"], spec["K"]
-        one = (N * K // 32 * 18) if spec["fmt"] == "q4_0" else (N * K + 4 * (N // 128) * (K // 128))
+        one = {"q4_0": N * K // 32 * 18, "q8_0": N * K // 32 * 34}.get(
+            spec["fmt"], N * K + 4 * (N // 128) * (K // 128))
         copies = args.copies or max(2, -(-4 * L2_BYTES // one))
         mats, spec = build_matrices(q, synth, shape_name, hadamard, copies, torch,
                                     splits=args.splits, kernel=args.kernel)
@@ -292,12 +302,12 @@ def run_gpu(args, ws, rank, local):
             items = [(m, act, outbuf[i]) for i, m in enumerate(mats)]
             groups.append((M, items))
         per_copy_bytes = one
-        fmt_name = "Q4_0" if spec["fmt"] == "q4_0" else "FP8 E4M3 128x128"
+        fmt_name = {"q4_0": "Q4_0", "q8_0": "Q8_0"}.get(spec["fmt"], "FP8 E4M3 128x128")
         rot = f" Hadamard{32 if hadamard is True else hadamard}" if hadamard else ""
         workload_desc = (f"{fmt_name} verify K={K} N={N}{rot}, "
                          f"M={'/'.join(map(str, Ms))}, {copies} distinct weight copies "
                          f"({copies * one / 1e6:.0f} MB, > 4x L2) cycled")
-        main_kernel = "verify_kernel<" + ("0" if spec["fmt"] == "q4_0" else "1")
+        main_kernel = "verify_kernel<" + {"q4_0": "0", "q8_0": "2"}.get(spec["fmt"], "1")
         dtype = "f16" if (hadamard or spec["fmt"] != "q4_0") else "bf16"
 
     # the greedy workload: per call the block's tokens (shared per M) and its
@@ -327,7 +337,7 @@ def run_gpu(args, ws, rank, local):
     calls_per_step = sum(len(items) for _, items in groups)
     rot_flags = q.QMM_FLAG_HADAMARD32 | q.QMM_FLAG_HADAMARD64 | q.QMM_FLAG_HADAMARD128
     launches_per_step = sum(sum(1 + int(bool(m.info()["flags"] & rot_flags)
-                                        or m.fmt == q.QMM_FMT_FP8_E4M3_B128)
+                                        or m.fmt != q.QMM_FMT_Q4_0)
                                 for m, _, _ in items) for _, items in groups)
     bytes_per_step = sum(sum(m.info()["weight_bytes"] for m, _, _ in items) for _, items in groups)
 
@@ -528,9 +538,14 @@ def oracle_sample_rate(budget_s: float, workload: str):
     N, K = spec["N"], spec["K"]
     rows_n = min(N, 512)
     w = synth.weights(rows_n, K, spec["seed"])
+    if hadamard:  # the offline rotation of the weights (32-, 64- or 128-point)
+        w = O.rotate_weights_f32(w, 32 if hadamard is True else int(hadamard))
     if spec["fmt"] == "q4_0":
-        wb = O.q4_0_quantize_h32(w) if hadamard else O.q4_0_quantize(w)
+        wb = O.q4_0_quantize(w)
         sc, fmt, row_bytes = None, O.FMT_Q4_0, K // 32 * 18
+    elif spec["fmt"] == "q8_0":
+        wb = O.q8_0_quantize(w)
+        sc, fmt, row_bytes = None, O.FMT_Q8_0, K // 32 * 34
     else:
         wb, sc = O.fp8_quantize(w)
         fmt, row_bytes = O.FMT_FP8, K

@@ -23,6 +23,14 @@
  *                          ["r9k: a from-scratch inference engine for
  *                          Qwen3.8-27B on two Radeon AI PRO R9700", opening
  *                          section].
+
+ *   QMM_FMT_Q8_0           32-element blocks, one fp16 scale d each, 8-bit
+ *                          two's-complement codes: W = d * q (the 8-bit
+ *                          reference format the pages name beside Q4_0,
+ *                          ["Qwen3.8-27B on the AMD R9700: up to 227 tok/s",
+ *                          TL;DR], read as the GGUF block layout of the same
+ *                          family).  Its activations always take the f16
+ *                          pre-pass, as FP8's do.
  * and optionally QMM_FLAG_HADAMARD32: every 32-block of each activation row is
  * rotated on the device by the unnormalised 32-point Walsh-Hadamard matrix H
  * (strides 1,2,4,8,16, each stage (x, y) -> (x + y, x - y), fp32), for weights
@@ -71,7 +79,7 @@ enum {
 };
 
 /* ---- formats and flags ---------------------------------------------------- */
-typedef enum { QMM_FMT_Q4_0 = 0, QMM_FMT_FP8_E4M3_B128 = 1 } qmm_format;
+typedef enum { QMM_FMT_Q4_0 = 0, QMM_FMT_FP8_E4M3_B128 = 1, QMM_FMT_Q8_0 = 2 } qmm_format;
 
 enum {
   /* Rotate each 32-block of the activations on the device (weights must have
@@ -97,7 +105,7 @@ typedef struct {
   uint32_t struct_size;      /* = sizeof(qmm_desc)                              */
   uint32_t format;           /* qmm_format                                      */
   int64_t N;                 /* output features (rows of W), N >= 1             */
-  int64_t K;                 /* input features; Q4_0: K % 32 == 0;
+  int64_t K;                 /* input features; Q4_0 and Q8_0: K % 32 == 0;
                                 FP8: N % 128 == 0 and K % 128 == 0              */
   uint32_t flags;            /* QMM_FLAG_*                                      */
   int32_t weights_on_device; /* 1: weights/scales are device pointers; 0: host  */
@@ -105,7 +113,10 @@ typedef struct {
                                 n then block: fp16 d (little endian), then 16 bytes
                                 where byte j holds element j in its low nibble and
                                 element j+16 in its high nibble.
-                                FP8: uint8 E4M3 codes [N][K], row-major.        */
+                                FP8: uint8 E4M3 codes [N][K], row-major.
+                                Q8_0: N*(K/32) blocks of 34 bytes, row-major over
+                                n then block: fp16 d (little endian), then the
+                                32 int8 codes in order.                          */
   const float* scales;       /* FP8: fp32 [N/128][K/128] row-major; Q4_0: NULL  */
   int32_t k_splits;          /* 0: the planner chooses; > 0: use this many K splits
                                 (tuning and tests; clamped to the stage count
@@ -122,7 +133,8 @@ typedef struct {
   uint32_t format, flags;
   int64_t N, K;
   int64_t weight_bytes;          /* compressed bytes of W as the format defines
-                                    them: Q4_0 N*K*18/32; FP8 N*K + 4*(N/128)*(K/128) */
+                                    them: Q4_0 N*K*18/32; Q8_0 N*K*34/32;
+                                    FP8 N*K + 4*(N/128)*(K/128)                 */
   int64_t device_weight_bytes;   /* bytes of the repacked device copy (with padding) */
   int64_t scratch_bytes;         /* per-handle scratch                          */
   int32_t n_tiles;               /* row tiles of the verify grid                */
@@ -275,6 +287,15 @@ int qmm_hadamard(const uint16_t* act, int64_t lda, float* act_out, int M, int64_
  * temporary fp32 copy of w allocated and freed in stream order on `stream`.
  * Async. */
 int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
+                      void* stream);
+
+/* Quantize fp32 weights w (device [N][K]) into Q8_0 blocks (device, N*(K/32)*34
+ * bytes, layout as in qmm_desc).  Per block: amax = largest |w|, d32 = amax /
+ * 127, q = clamp(roundf(w * (1/d32)), -127, 127) (0 for an all-zero block),
+ * stored d = fp16 round-to-nearest-even of d32.  The rotation flags rotate
+ * first, as for qmm_quantize_q4_0 (through a stream-ordered temporary).
+ * K % 32 == 0.  Async. */
+int qmm_quantize_q8_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
                       void* stream);
 
 /* Quantize fp32 weights w (device [N][K]) to E4M3 codes (device [N][K]) and

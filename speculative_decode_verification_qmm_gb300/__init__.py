@@ -16,7 +16,7 @@ import ctypes
 
 from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_ARG,
                    QMM_ERR_M_RANGE, QMM_ERR_SHAPE, QMM_ERR_STATE, QMM_ERR_TIMEOUT,
-                   QMM_FLAG_HADAMARD32, QMM_FLAG_HADAMARD64, QMM_FLAG_HADAMARD128, QMM_FLAG_TCGEN05, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0,
+                   QMM_FLAG_HADAMARD32, QMM_FLAG_HADAMARD64, QMM_FLAG_HADAMARD128, QMM_FLAG_TCGEN05, QMM_FLAG_SIMT, QMM_FMT_FP8_E4M3_B128, QMM_FMT_Q4_0, QMM_FMT_Q8_0,
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
@@ -27,7 +27,7 @@ __all__ = [
     "QmmError", "load",
     "QMM_OK", "QMM_ERR_INVALID_ARG", "QMM_ERR_SHAPE", "QMM_ERR_M_RANGE", "QMM_ERR_ALIGN",
     "QMM_ERR_CUDA", "QMM_ERR_TIMEOUT", "QMM_ERR_STATE", "QMM_ERR_DEVICE",
-    "QMM_FMT_Q4_0", "QMM_FMT_FP8_E4M3_B128", "QMM_FLAG_HADAMARD32", "QMM_FLAG_SIMT",
+    "QMM_FMT_Q4_0", "QMM_FMT_FP8_E4M3_B128", "QMM_FMT_Q8_0", "qmm_quantize_q8_0", "quantize_q8_0", "QMM_FLAG_HADAMARD32", "QMM_FLAG_SIMT",
     "QMM_FLAG_TCGEN05", "QMM_FLAG_HADAMARD64", "QMM_FLAG_HADAMARD128", "qmm_hadamard",
     "rotation_flag", "hadamard",
 ]
@@ -168,6 +168,12 @@ def qmm_quantize_q4_0(w, blocks, flags: int = 0, stream=None) -> None:
                                                          _stream_ptr(stream)))
 
 
+def qmm_quantize_q8_0(w, blocks, flags: int = 0, stream=None) -> None:
+    N, K = w.shape
+    _check("qmm_quantize_q8_0", load().qmm_quantize_q8_0(_ptr(w), N, K, flags, _ptr(blocks),
+                                                         _stream_ptr(stream)))
+
+
 def qmm_quantize_fp8(w, codes, scales, flags: int = 0, stream=None) -> None:
     N, K = w.shape
     _check("qmm_quantize_fp8", load().qmm_quantize_fp8(_ptr(w), N, K, flags, _ptr(codes),
@@ -190,6 +196,15 @@ def quantize_q4_0(w, hadamard=False, stream=None):
     N, K = w.shape
     blocks = torch.empty((N, K // 32, 18), dtype=torch.uint8, device=w.device)
     qmm_quantize_q4_0(w.contiguous(), blocks, rotation_flag(hadamard), stream)
+    return blocks
+
+
+def quantize_q8_0(w, hadamard=False, stream=None):
+    """CUDA fp32 [N, K] -> CUDA uint8 [N, K/32, 34] Q8_0 blocks (device quantizer)."""
+    import torch
+    N, K = w.shape
+    blocks = torch.empty((N, K // 32, 34), dtype=torch.uint8, device=w.device)
+    qmm_quantize_q8_0(w.contiguous(), blocks, rotation_flag(hadamard), stream)
     return blocks
 
 

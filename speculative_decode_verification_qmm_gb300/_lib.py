@@ -22,6 +22,7 @@ QMM_ERR_DEVICE = 8
 
 QMM_FMT_Q4_0 = 0
 QMM_FMT_FP8_E4M3_B128 = 1
+QMM_FMT_Q8_0 = 2
 QMM_FLAG_HADAMARD32 = 1
 QMM_FLAG_SIMT = 2
 QMM_FLAG_TCGEN05 = 4
@@ -85,6 +86,7 @@ SIGNATURES = {
     "qmm_hadamard32": (_INT, [_P, _I64, _P, _INT, _I64, _P]),
     "qmm_hadamard": (_INT, [_P, _I64, _P, _INT, _I64, _INT, _P]),
     "qmm_quantize_q4_0": (_INT, [_P, _I64, _I64, _U32, _P, _P]),
+    "qmm_quantize_q8_0": (_INT, [_P, _I64, _I64, _U32, _P, _P]),
     "qmm_quantize_fp8": (_INT, [_P, _I64, _I64, _U32, _P, _P, _P]),
     "qmm_debug_set_wait_limit": (_INT, [_P, _I64]),
     "qmm_debug_fail_allocs": (_INT, [_INT]),

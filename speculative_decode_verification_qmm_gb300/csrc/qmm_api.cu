@@ -30,7 +30,10 @@ constexpr size_t GREEDY_STATE_BYTES = MAX_M * sizeof(unsigned long long) + 16;
 constexpr double PLAN_HBM_BPS = 6.8e12;
 constexpr double PLAN_CTA_BPS = 30e9;
 constexpr double PLAN_CLUSTER_REDUCE_S = 0.4e-6;
-constexpr double PLAN_STAGE_1_S = 0.35e-6;
+// a CTA alone on its SM streams ~0.67 us per stage over a long range (Q8_0 and
+// FP8, 17408 x 5120: 40 stages in 26.7 us), so a grid of one CTA per SM only
+// wins when the stages per CTA are few
+constexpr double PLAN_STAGE_1_S = 0.65e-6;
 constexpr double PLAN_STAGE_2_S = 0.50e-6;
 constexpr double PLAN_FIXED_S = 1.5e-6;
 constexpr double PLAN_FIXUP_S = 0.8e-6;
@@ -144,9 +147,10 @@ int rotation_block(uint32_t flags) {
 Plan make_plan(int fmt, bool tc, int64_t N, int64_t K, int sm_count, int forced_splits) {
   Plan p;
   p.tc = tc;
-  p.stage_k = fmt == 0 ? Q4_STAGE_K : F8_STAGE_K;
-  p.stage_bytes = fmt == 0 ? Q4_STAGE_BYTES : F8_STAGE_BYTES;
-  p.depth = tc ? tc_pipeline_depth() : (fmt == 0 ? q4_pipeline_depth() : fp8_pipeline_depth());
+  p.stage_k = fmt == 0 ? Q4_STAGE_K : (fmt == 2 ? Q8_STAGE_K : F8_STAGE_K);
+  p.stage_bytes = fmt == 0 ? Q4_STAGE_BYTES : (fmt == 2 ? Q8_STAGE_BYTES : F8_STAGE_BYTES);
+  p.depth = tc ? tc_pipeline_depth()
+               : (fmt == 0 ? q4_pipeline_depth() : (fmt == 2 ? q8_pipeline_depth() : fp8_pipeline_depth()));
   p.n_tiles = (int)ceil_div(N, TILE_N);
   p.nst = ceil_div(K, p.stage_k);
   auto fix = [&](int S) {
@@ -315,7 +319,8 @@ cudaError_t launch_verify_kernel(qmm_handle* h, const VerifyParams& vp, const Ve
   cudaError_t e = act_map_for(h, rows, lda, M, f16, &map);
   if (e != cudaSuccess) return e;
   if (h->plan.tc) return launch_verify_tc(vp, map, false, vl.ctas, vl.stream);
-  return h->fmt == 0 ? launch_verify_q4(vp, vl, map) : launch_verify_fp8(vp, vl, map);
+  if (h->fmt == 0) return launch_verify_q4(vp, vl, map);
+  return h->fmt == 2 ? launch_verify_q8(vp, vl, map) : launch_verify_fp8(vp, vl, map);
 }
 
 }  // namespace
@@ -347,7 +352,8 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   if (!out) return QMM_ERR_INVALID_ARG;
   *out = nullptr;
   if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
-  if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
+  if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128 && d->format != QMM_FMT_Q8_0)
+    return QMM_ERR_INVALID_ARG;
   if (d->flags & ~(uint32_t)(ROTATION_FLAGS | QMM_FLAG_SIMT | QMM_FLAG_TCGEN05))
     return QMM_ERR_INVALID_ARG;
   const int rb = rotation_block(d->flags);
@@ -355,13 +361,13 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   if (d->k_splits < 0) return QMM_ERR_INVALID_ARG;
   const int fmt = (int)d->format;
   if (fmt == 1 && !d->scales) return QMM_ERR_INVALID_ARG;
-  if (fmt == 1 && (d->flags & QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
+  if (fmt != 0 && (d->flags & QMM_FLAG_SIMT)) return QMM_ERR_INVALID_ARG;
   // the tcgen05 kernel serves bf16 Q4_0 only: no rotation, not the CUDA-core baseline
   if ((d->flags & QMM_FLAG_TCGEN05) &&
       (fmt != 0 || (d->flags & (ROTATION_FLAGS | QMM_FLAG_SIMT))))
     return QMM_ERR_INVALID_ARG;
   if (d->N < 1 || d->K < 1) return QMM_ERR_SHAPE;
-  if (fmt == 0 && d->K % 32) return QMM_ERR_SHAPE;
+  if ((fmt == 0 || fmt == 2) && d->K % 32) return QMM_ERR_SHAPE;
   if (fmt == 1 && (d->N % 128 || d->K % 128)) return QMM_ERR_SHAPE;
   if (rb > 0 && d->K % rb) return QMM_ERR_SHAPE;
   if (d->N > (1ll << 31) || d->K > (1ll << 31)) return QMM_ERR_SHAPE;
@@ -381,7 +387,8 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   // tcgen05 kernel for bf16 Q4_0 (checked above).
   const bool tc = (d->flags & QMM_FLAG_TCGEN05) != 0;
   cudaError_t e = tc ? prepare_tc_attributes()
-                     : (fmt == 0 ? prepare_q4_attributes() : prepare_fp8_attributes());
+                     : (fmt == 0 ? prepare_q4_attributes()
+                                 : (fmt == 2 ? prepare_q8_attributes() : prepare_fp8_attributes()));
   if (e != cudaSuccess) {
     free_handle(h);
     return cuda_fail(nullptr, e);
@@ -423,7 +430,9 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
 
   const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(d->weights);
   const float* ssrc = d->scales;
-  const size_t wbytes = fmt == 0 ? (size_t)d->N * (d->K / 32) * 18 : (size_t)d->N * d->K;
+  const size_t wbytes = fmt == 0   ? (size_t)d->N * (d->K / 32) * 18
+                        : fmt == 2 ? (size_t)d->N * (d->K / 32) * 34
+                                   : (size_t)d->N * d->K;
   const size_t sbytes = fmt == 1 ? (size_t)(d->N / 128) * (d->K / 128) * sizeof(float) : 0;
   if (!d->weights_on_device) {
     QMM_ALLOC(tmp_w, wbytes);
@@ -503,7 +512,7 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   const Plan& p = h->plan;
   const int hb = rotation_block(h->flags);
   const bool had = hb > 0;
-  const bool f16 = had || h->fmt == 1;
+  const bool f16 = had || h->fmt != 0;
   // bf16 operands read the caller's rows directly; the f16 paths (Hadamard
   // rotation, FP8) go through the activation pre-pass and its scratch.
   cudaError_t e = cudaSuccess;
@@ -634,8 +643,9 @@ int qmm_get_info(qmm_t h, qmm_info* info) {
   info->flags = h->flags;
   info->N = h->N;
   info->K = h->K;
-  info->weight_bytes = h->fmt == 0 ? h->N * h->K / 32 * 18
-                                   : h->N * h->K + 4 * (h->N / 128) * (h->K / 128);
+  info->weight_bytes = h->fmt == 0   ? h->N * h->K / 32 * 18
+                       : h->fmt == 2 ? h->N * h->K / 32 * 34
+                                     : h->N * h->K + 4 * (h->N / 128) * (h->K / 128);
   info->device_weight_bytes = (int64_t)h->wdev_bytes;
   info->scratch_bytes = (int64_t)(h->act_bytes + MAX_M * p.S * sizeof(float) + sizeof(int)) +
                         (h->ws ? (int64_t)p.n_tiles * p.S * MAX_M * TILE_N * 4 + (int64_t)p.n_tiles * 4 : 0);
@@ -726,6 +736,26 @@ int qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint
   return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
 }
 
+int qmm_quantize_q8_0(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* blocks,
+                      void* stream) {
+  if (!w || !blocks) return QMM_ERR_INVALID_ARG;
+  if (flags & ~ROTATION_FLAGS) return QMM_ERR_INVALID_ARG;
+  const int rb = rotation_block(flags);
+  if (rb < 0) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32 || (rb > 0 && K % rb)) return QMM_ERR_SHAPE;
+  if ((uintptr_t)w & 15) return QMM_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  int rc = check_device(&dev, &sms);
+  if (rc != QMM_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+  if (rb > 0)
+    e = quantize_rotated(w, N, K, rb, st, [&](const float* r) { return launch_quantize_q8(r, N, K, blocks, st); });
+  else
+    e = launch_quantize_q8(w, N, K, blocks, st);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(nullptr, e);
+}
+
 int qmm_quantize_fp8(const float* w, int64_t N, int64_t K, uint32_t flags, uint8_t* codes,
                      float* scales, void* stream) {
   if (!w || !codes || !scales) return QMM_ERR_INVALID_ARG;
@@ -803,7 +833,7 @@ extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, flo
   const Plan& p = h->plan;
   const int hb = rotation_block(h->flags);
   const bool had = hb > 0;
-  const bool f16 = had || h->fmt == 1;
+  const bool f16 = had || h->fmt != 0;
   // Carve the array: activation scratch | per-(row, split) factors.  Both are
   // written in full by the pre-pass before the verify kernel reads them, so
   // nothing has to be cleared; the bf16 path reads the caller's rows and uses

@@ -257,6 +257,58 @@ __global__ void repack_fp8_kernel(const uint8_t* __restrict__ codes, const float
   }
 }
 
+// Q8_0 canonical blocks (34 bytes: fp16 d, 32 int8 codes) -> stage units:
+// the codes in the FP8 unit's order, stored as q + 128; lanes 0..7 also store
+// the (d[g], d[g + 8]) pair of rows g, g + 8 of the unit.  Padding rows and
+// columns hold code 0 (stored 128) and scale 0.
+__global__ void repack_q8_kernel(const uint8_t* __restrict__ blocks, int64_t N, int64_t K, int S,
+                                 int spc, int64_t total_units, uint8_t* __restrict__ wdev) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
+  const int64_t stage_global = u;
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t nb = K / 32;
+  const int64_t kbase = ((int64_t)split * spc + i) * Q8_STAGE_K + 32 * c;
+  uint32_t words[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int j = v >> 1, h = v & 1;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int a = 2 * h + (e >> 1);
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (a & 1);
+      const int64_t k = kbase + 16 * j + 2 * t + (e & 1) + 8 * (a >> 1);
+      const uint32_t code = (n < N && k < K) ? blocks[(n * nb + k / 32) * 34 + 2 + k % 32] : 0u;
+      w |= (code ^ 0x80u) << (8 * e);
+    }
+    words[v] = w;
+  }
+  uint8_t* unit = wdev + stage_global * Q8_STAGE_BYTES + (int64_t)(c * 8 + r) * Q8_UNIT_BYTES;
+  *reinterpret_cast<uint4*>(unit + 16 * lane) = make_uint4(words[0], words[1], words[2], words[3]);
+  if (lane < 8) {
+    uint32_t pair = 0;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int64_t n = tile * TILE_N + 16 * r + lane + 8 * hh;
+      uint32_t d = 0;
+      if (n < N && kbase < K) {
+        const uint8_t* blk = blocks + (n * nb + kbase / 32) * 34;
+        d = (uint32_t)blk[0] | ((uint32_t)blk[1] << 8);
+      }
+      pair |= d << (16 * hh);
+    }
+    *reinterpret_cast<uint32_t*>(unit + 512 + 4 * lane) = pair;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Exact dequantization from the repacked stream (test hook): one thread per
 // (unit, lane) decodes its 16 bytes back to (n, k) positions.
@@ -292,6 +344,41 @@ __global__ void dequant_q4_kernel(const uint8_t* __restrict__ wdev, int64_t N, i
         const uint16_t dbits = (uint16_t)((pair & 1) ? (dp >> 16) : (dp & 0xFFFF));
         const int q = (int)((words[v] >> (4 * pn)) & 15u);
         out[n * K + k] = __half2float(__ushort_as_half(dbits)) * (float)(q - 8);
+      }
+    }
+  }
+}
+
+__global__ void dequant_q8_kernel(const uint8_t* __restrict__ wdev, int64_t N, int64_t K, int S, int spc,
+                                  int64_t total_units, float* __restrict__ out) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= total_units * 32) return;
+  const int lane = (int)(gt & 31);
+  int64_t u = gt >> 5;
+  const int r = (int)(u % 8); u /= 8;
+  const int c = (int)(u % STAGE_CHUNKS); u /= STAGE_CHUNKS;
+  const int64_t stage_global = u;
+  const int i = (int)(u % spc); u /= spc;
+  const int split = (int)(u % S);
+  const int64_t tile = u / S;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t kbase = ((int64_t)split * spc + i) * Q8_STAGE_K + 32 * c;
+  const uint8_t* unit = wdev + stage_global * Q8_STAGE_BYTES + (int64_t)(c * 8 + r) * Q8_UNIT_BYTES;
+  const uint4 cw = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+  const uint32_t dpair = *reinterpret_cast<const uint32_t*>(unit + 512 + 4 * g);
+  const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int j = v >> 1, h = v & 1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int a = 2 * h + (e >> 1);
+      const int64_t n = tile * TILE_N + 16 * r + g + 8 * (a & 1);
+      const int64_t k = kbase + 16 * j + 2 * t + (e & 1) + 8 * (a >> 1);
+      if (n < N && k < K) {
+        const uint16_t dbits = (uint16_t)((a & 1) ? (dpair >> 16) : (dpair & 0xFFFF));
+        const int q = (int)((words[v] >> (8 * e)) & 0xFFu) - 128;
+        out[n * K + k] = __half2float(__ushort_as_half(dbits)) * (float)q;
       }
     }
   }
@@ -341,8 +428,8 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, const float
 // ---------------------------------------------------------------------------
 // Quantizers (offline tools).
 // ---------------------------------------------------------------------------
-// The offline weight rotation of the 64- and 128-point variants, ahead of the
-// plain quantizers: every HB-block of a row of w [N][K] fp32 rotated with
+// The offline weight rotation ahead of the plain quantizers (the 64- and
+// 128-point variants, and every rotation of Q8_0): every HB-block of a row of w [N][K] fp32 rotated with
 // fwht_lanes and multiplied by 1/HB (a power of two, exact) into out.
 template <int HB>
 __global__ void __launch_bounds__(256) rotate_weights_kernel(const float* __restrict__ w, int64_t N,
@@ -435,6 +522,40 @@ __global__ void quantize_q4_kernel(const float* __restrict__ w, int64_t N, int64
     const unsigned int lo = (unsigned int)q[2 * j] | ((unsigned int)q[2 * j + 16] << 4);
     const unsigned int hi = (unsigned int)q[2 * j + 1] | ((unsigned int)q[2 * j + 17] << 4);
     dst[1 + j] = (unsigned short)(lo | (hi << 8));
+  }
+}
+
+// Q8_0: one thread per 32-block.  amax = largest |x|, d32 = amax / 127,
+// inv = 1 / d32 (0 for an all-zero block), q = clamp(round half away from zero
+// of x * inv, -127, 127), stored d = fp16_rne(d32); 34-byte blocks start on
+// even addresses, so the block is written as 17 aligned 16-bit words.
+__global__ void quantize_q8_kernel(const float* __restrict__ w, int64_t N, int64_t K,
+                                   uint8_t* __restrict__ blocks) {
+  const int64_t nb = K / 32;
+  const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (id >= N * nb) return;
+  const int64_t n = id / nb, b = id % nb;
+  float x[32];
+  const float4* src = reinterpret_cast<const float4*>(w + n * K + 32 * b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = src[i];
+    x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float d32 = __fdiv_rn(amax, 127.0f);
+  const float inv = (d32 != 0.f) ? __fdiv_rn(1.0f, d32) : 0.f;
+  unsigned short* dst = reinterpret_cast<unsigned short*>(blocks + id * 34);
+  dst[0] = __half_as_ushort(__float2half_rn(d32));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    int q0 = round_half_away(__fmul_rn(x[2 * j], inv));
+    int q1 = round_half_away(__fmul_rn(x[2 * j + 1], inv));
+    q0 = q0 < -127 ? -127 : (q0 > 127 ? 127 : q0);
+    q1 = q1 < -127 ? -127 : (q1 > 127 ? 127 : q1);
+    dst[1 + j] = (unsigned short)(((unsigned)q0 & 0xFFu) | (((unsigned)q1 & 0xFFu) << 8));
   }
 }
 
@@ -547,7 +668,7 @@ cudaError_t launch_hadamard(const uint16_t* act, int64_t lda, float* out, int M,
   return cudaGetLastError();
 }
 
-// w rotated in hb-blocks (hb = 64 or 128) and times 1/hb into out (fp32 [N][K]).
+// w rotated in hb-blocks (hb = 32, 64 or 128) and times 1/hb into out (fp32 [N][K]).
 cudaError_t launch_rotate_weights(const float* w, int64_t N, int64_t K, int hb, float* out,
                                   cudaStream_t st) {
   const int64_t work = (K / 128 + 1) * N;
@@ -556,8 +677,10 @@ cudaError_t launch_rotate_weights(const float* w, int64_t N, int64_t K, int hb, 
   if (blocks < 1) blocks = 1;
   if (hb == 128)
     rotate_weights_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, out);
-  else
+  else if (hb == 64)
     rotate_weights_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, out);
+  else
+    rotate_weights_kernel<32><<<(unsigned)blocks, 256, 0, st>>>(w, N, K, out);
   return cudaGetLastError();
 }
 
@@ -569,6 +692,8 @@ cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)
     repack_q4_kernel<<<blocks, 256, 0, st>>>(wsrc, N, K, S, spc, units, wdev);
+  else if (fmt == 2)
+    repack_q8_kernel<<<blocks, 256, 0, st>>>(wsrc, N, K, S, spc, units, wdev);
   else
     repack_fp8_kernel<<<blocks, 256, 0, st>>>(wsrc, scales, N, K, S, spc, units, wdev, f8_scale);
   return cudaGetLastError();
@@ -581,6 +706,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t* wdev, const float* f8_scale, 
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fmt == 0)
     dequant_q4_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
+  else if (fmt == 2)
+    dequant_q8_kernel<<<blocks, 256, 0, st>>>(wdev, N, K, S, spc, units, out);
   else
     dequant_fp8_kernel<<<blocks, 256, 0, st>>>(wdev, f8_scale, N, K, S, spc, units, out);
   return cudaGetLastError();
@@ -591,6 +718,13 @@ cudaError_t launch_quantize_q4(const float* w, int64_t N, int64_t K, int had, ui
   const int64_t n = N * (K / 32);
   if (n == 0) return cudaSuccess;
   quantize_q4_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(w, N, K, had, blocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q8(const float* w, int64_t N, int64_t K, uint8_t* blocks, cudaStream_t st) {
+  const int64_t n = N * (K / 32);
+  if (n == 0) return cudaSuccess;
+  quantize_q8_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(w, N, K, blocks);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,12 @@ constexpr int F8_STAGE_K = 128;
 constexpr int F8_UNIT_BYTES = 512;
 constexpr int F8_CHUNK_BYTES = 8 * F8_UNIT_BYTES;                  // 4096
 constexpr int F8_STAGE_BYTES = STAGE_CHUNKS * F8_CHUNK_BYTES;      // 16384
+// Q8_0: a unit is 16 rows x 32 columns (one block per row): 512 code bytes in
+// the FP8 unit's order, stored as q + 128, then 8 x (d[g], d[g + 8]) fp16 pairs
+constexpr int Q8_STAGE_K = 128;
+constexpr int Q8_UNIT_BYTES = 544;
+constexpr int Q8_CHUNK_BYTES = 8 * Q8_UNIT_BYTES;                  // 4352
+constexpr int Q8_STAGE_BYTES = STAGE_CHUNKS * Q8_CHUNK_BYTES;      // 17408
 
 // Device error word bits (OR-ed into the handle's status word).
 constexpr int DEV_ERR_TIMEOUT_FULL = 1;   // consumer gave up waiting for a stage
@@ -268,6 +274,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 

@@ -21,6 +21,9 @@ struct VerifyLaunch {
 // kernels' shared-memory attribute (set on the current device).
 int q4_pipeline_depth();
 int fp8_pipeline_depth();
+int q8_pipeline_depth();
+size_t q8_smem_bytes();
+cudaError_t prepare_q8_attributes();
 size_t q4_smem_bytes();
 size_t fp8_smem_bytes();
 cudaError_t prepare_q4_attributes();
@@ -44,6 +47,7 @@ cudaError_t launch_dequant_tc(const uint8_t* wdev, int64_t N, int64_t K, int n_t
 // with boxes of 8 values x R rows x chunk columns / 8, R = 8 for M <= 8, else 16.
 cudaError_t launch_verify_q4(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
 cudaError_t launch_verify_fp8(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
+cudaError_t launch_verify_q8(const VerifyParams& p, const VerifyLaunch& l, const void* act_map);
 
 // The activation pre-pass of the f16 operand paths; hb = rotation block size
 // (0 none, 32, 64, 128).
@@ -51,7 +55,7 @@ cudaError_t launch_act_prep(const PrepParams& p, bool out_f16, int hb, cudaStrea
 // Rotation of activation rows in hb-blocks (32, 64, 128) to fp32.
 cudaError_t launch_hadamard(const uint16_t* act, int64_t lda, float* out, int M, int64_t K, int hb,
                             int sm_count, cudaStream_t st);
-// Offline weight rotation in hb-blocks (64, 128), times 1/hb.
+// Offline weight rotation in hb-blocks (32, 64, 128), times 1/hb.
 cudaError_t launch_rotate_weights(const float* w, int64_t N, int64_t K, int hb, float* out,
                                   cudaStream_t st);
 cudaError_t launch_repack(int fmt, const uint8_t* wsrc, const float* scales, int64_t N, int64_t K,
@@ -61,6 +65,7 @@ cudaError_t launch_dequant(int fmt, const uint8_t* wdev, const float* f8_scale, 
                            int n_tiles, int S, int spc, float* out, cudaStream_t st);
 cudaError_t launch_quantize_q4(const float* w, int64_t N, int64_t K, int had, uint8_t* blocks,
                                cudaStream_t st);
+cudaError_t launch_quantize_q8(const float* w, int64_t N, int64_t K, uint8_t* blocks, cudaStream_t st);
 cudaError_t launch_quantize_fp8(const float* w, int64_t N, int64_t K, int had, uint8_t* codes,
                                 float* scales, cudaStream_t st);
 

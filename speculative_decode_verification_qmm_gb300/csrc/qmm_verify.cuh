@@ -53,6 +53,15 @@ struct FmtTraits<1> {  // FP8 E4M3, 128x128 scales
   static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 32
 };
 
+template <>
+struct FmtTraits<2> {  // Q8_0
+  static constexpr int STAGE_K = Q8_STAGE_K;
+  static constexpr int STAGE_BYTES = Q8_STAGE_BYTES;
+  static constexpr int CHUNK_BYTES = Q8_CHUNK_BYTES;
+  static constexpr int UNIT_BYTES = Q8_UNIT_BYTES;
+  static constexpr int CHUNK_K = STAGE_K / STAGE_CHUNKS;  // 32: one Q8_0 block
+};
+
 // Row subtiles (16 rows) per compute warp: the 8 subtiles of a tile are split
 // into two halves.
 constexpr int WARP_SUBTILES = 8 * STAGE_CHUNKS / COMPUTE_WARPS;  // 4
@@ -189,6 +198,57 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
         ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
         ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);
       }
+    }
+  }
+}
+
+// Q8_0 codes stored as u = q + 128, two bytes -> f16x2 (1024 + u, exact) by
+// one byte permute: result bytes (b_lo, 0x64, b_hi, 0x64).
+__device__ __forceinline__ uint32_t u8x2_to_f16x2_biased(uint32_t w, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0x64646464u), "r"(sel));
+  return r;
+}
+
+// Q8_0: the chunk's 32 columns are one block per row.  The weights enter the
+// MMA as 1152 + q (f16, exact) and each block's accumulator starts at
+// -1152 * sum_k a[m][k] (an MMA with a constant A operand), so the block sum
+// is sum q a without a subtraction per weight; the block scale d (per row)
+// is then applied with packed fp32 FMAs, as for Q4_0.
+template <int NT8>
+__device__ __forceinline__ void q8_stage_mma(uint32_t wunit0, uint32_t abase, int lane,
+                                             float (&acc)[WARP_SUBTILES][2][4]) {
+  const int g = lane >> 2;
+  uint32_t b[2][4];
+  load_b_frags<2, 8 * NT8, 2 * Q8_STAGE_K / STAGE_CHUNKS>(abase, lane, b);
+  float c0[NT8][4];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c0[j][e] = 0.f;
+    constexpr uint32_t kNeg1152 = 0xE480E480u;  // f16x2 (-1152, -1152)
+    F16Op::mma(c0[j], kNeg1152, kNeg1152, kNeg1152, kNeg1152, b[0][2 * j], b[0][2 * j + 1], c0[j]);
+    F16Op::mma(c0[j], kNeg1152, kNeg1152, kNeg1152, kNeg1152, b[1][2 * j], b[1][2 * j + 1], c0[j]);
+  }
+#pragma unroll
+  for (int r = 0; r < WARP_SUBTILES; ++r) {
+    const uint32_t unit = wunit0 + (uint32_t)(r * Q8_UNIT_BYTES);
+    const uint4 codes = lds128(unit + 16u * lane);
+    const uint32_t dpair = lds32(unit + 512u + 4u * g);  // (d[g], d[g + 8])
+    // word v: k16 step v / 2, half v % 2 -> A registers (a0, a1) or (a2, a3)
+    const uint32_t a00 = u8x2_to_f16x2_biased(codes.x, 0x4140u), a01 = u8x2_to_f16x2_biased(codes.x, 0x4342u);
+    const uint32_t a02 = u8x2_to_f16x2_biased(codes.y, 0x4140u), a03 = u8x2_to_f16x2_biased(codes.y, 0x4342u);
+    const uint32_t a10 = u8x2_to_f16x2_biased(codes.z, 0x4140u), a11 = u8x2_to_f16x2_biased(codes.z, 0x4342u);
+    const uint32_t a12 = u8x2_to_f16x2_biased(codes.w, 0x4140u), a13 = u8x2_to_f16x2_biased(codes.w, 0x4342u);
+    const float dg = __half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF)));
+    const float dg8 = __half2float(__ushort_as_half((unsigned short)(dpair >> 16)));
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      float pp[4];
+      F16Op::mma(pp, a00, a01, a02, a03, b[0][2 * j], b[0][2 * j + 1], c0[j]);
+      F16Op::mma(pp, a10, a11, a12, a13, b[1][2 * j], b[1][2 * j + 1], pp);
+      ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
+      ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);
     }
   }
 }
@@ -346,7 +406,7 @@ static __device__ __noinline__ void greedy_tile(const VerifyParams& p, const flo
 
 // ---------------------------------------------------------------------------
 // The kernel.
-//   FMT  0 = Q4_0, 1 = FP8
+//   FMT  0 = Q4_0, 1 = FP8, 2 = Q8_0
 //   Op   Bf16Op or F16Op (FP8 always F16Op)
 //   NT8  1 for M <= 8, 2 for M <= 16 (R = 8 * NT8 activation rows staged)
 //   SIMT true: CUDA-core baseline compute (Q4_0 only)
@@ -492,8 +552,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         const uint32_t ach = s_a + slot * L::A_STAGE + chunk * L::A_CHUNK;
         if constexpr (FMT == 0)
           q4_stage_mma<Op, NT8>(wch, ach, lane, acc);
-        else
+        else if constexpr (FMT == 1)
           f8_stage_mma<NT8>(wch, ach, fs, lane, acc);
+        else
+          q8_stage_mma<NT8>(wch, ach, lane, acc);
         __syncwarp();
         if (lane == 0) release(i, chunk);
         __syncwarp();

@@ -177,3 +177,27 @@ def test_activation_recipe():
     assert (synth.activations(16, 5120, 1001, outliers=True, outlier_seed=2001) == a).all()
     w = synth.weights(64, 256, 5)
     assert w.dtype == np.float32 and abs(w.std() - 0.02) < 0.002
+
+
+def test_q8_0_host_validation(L):
+    """Q8_0 descriptions are validated before any CUDA call: K % 32, no
+    CUDA-core or tcgen05 kernel, and the quantizer's shape and flag checks."""
+    h = ctypes.c_void_p()
+    d = _lib.qmm_desc()
+    d.struct_size = ctypes.sizeof(d)
+    w = np.zeros(34 * 8, np.uint8)
+    d.weights = w.ctypes.data
+    d.format = q.QMM_FMT_Q8_0
+    d.N, d.K = 8, 48
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_SHAPE
+    d.K = 32
+    d.flags = q.QMM_FLAG_SIMT
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_TCGEN05
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_INVALID_ARG
+    d.flags = q.QMM_FLAG_HADAMARD64
+    assert L.qmm_create(ctypes.byref(h), ctypes.byref(d), None) == q.QMM_ERR_SHAPE  # K % 64
+    assert h.value is None
+    assert L.qmm_quantize_q8_0(None, 4, 32, 0, None, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize_q8_0(w.ctypes.data, 4, 40, 0, w.ctypes.data, None) == q.QMM_ERR_SHAPE
+    assert L.qmm_quantize_q8_0(w.ctypes.data, 4, 64, q.QMM_FLAG_SIMT, w.ctypes.data, None) == q.QMM_ERR_INVALID_ARG
