@@ -70,7 +70,7 @@ enum {
   QMM_OK = 0,
   QMM_ERR_INVALID_ARG = 1, /* NULL pointer, bad enum, bad struct_size, bad flag */
   QMM_ERR_SHAPE = 2,       /* N or K not accepted by the format (see qmm_desc)   */
-  QMM_ERR_M_RANGE = 3,     /* M outside [1, 16]                                 */
+  QMM_ERR_M_RANGE = 3,     /* M outside [1, 16] (prefill: [1, QMM_PREFILL_MAX_M]) */
   QMM_ERR_ALIGN = 4,       /* pointer alignment or leading dimension rejected   */
   QMM_ERR_CUDA = 5,        /* a CUDA call failed; see qmm_last_cuda_error()     */
   QMM_ERR_TIMEOUT = 6,     /* a bounded device wait expired (qmm_sync_status)   */
@@ -240,11 +240,47 @@ int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_h
 int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
                        int M, void* stream);
 
+/* ---- the prefill product --------------------------------------------------------- */
+
+/* The same product for a prompt's worth of rows, on an FP8 handle:
+ *     out[m][n] = sum_k act[m][k] * W[n][k]       1 <= M <= QMM_PREFILL_MAX_M
+ * the block-scaled FP8 GEMM that processes the prompt ["r9k: a from-scratch
+ * inference engine for Qwen3.8-27B on two Radeon AI PRO R9700", opening
+ * section: prefill runs through a custom block-scaled FP8 GEMM over the
+ * 128 x 128-scaled E4M3 weights].  It reads the handle's weights as they are
+ * (no second copy) and runs on the tcgen05 tensor cores: each activation row
+ * (rotated first for the Hadamard flags) is scaled by a power of two 2^e that
+ * brings its largest magnitude into [2^14, 2^15), rounded to f16 and written
+ * to the workspace; the codes are converted to f16 exactly; every 128 x 128
+ * tile product is accumulated in fp32, multiplied by its tile's scale and
+ * added in fp32, and the row's sum is multiplied by 2^-e.  The result is held
+ * to the same tolerance as qmm_verify.
+ *   act : device, bf16 bits, row m at act + m*lda; 16-byte aligned, lda >= K,
+ *         lda % 8 == 0.
+ *   out : device, fp32, row m at out + m*ldo; 16-byte aligned, ldo >= N.  Rows
+ *         0..M-1 fully overwritten.
+ *   workspace : device, 256-byte aligned, at least the bytes
+ *         qmm_prefill_workspace() gives for M; owned by the caller, used only
+ *         while the call's kernels run on `stream` (the f16 rows, then their
+ *         multipliers).
+ * Asynchronous on `stream` (two kernels: the pre-pass and the GEMM).
+ * Errors: STATE, INVALID_ARG (not an FP8 handle, NULL act/out/workspace,
+ * workspace too small), M_RANGE, ALIGN, DEVICE, CUDA (launch). */
+#define QMM_PREFILL_MAX_M (1 << 22)
+int qmm_prefill(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int64_t M,
+                void* workspace, int64_t workspace_bytes, void* stream);
+
+/* *bytes = the workspace qmm_prefill needs for M rows (M * K * 2 rounded up to
+ * 256, plus M * 4).  Errors: INVALID_ARG (NULL bytes, not an FP8 handle),
+ * STATE, M_RANGE. */
+int qmm_prefill_workspace(qmm_t h, int64_t M, int64_t* bytes);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Wait for `stream`, then read and clear the handle's device error word.
- * Returns QMM_OK, QMM_ERR_TIMEOUT (a kernel gave up on a bounded wait; its
- * output is undefined and the handle's device state has been reset), or
+ * Returns QMM_OK, QMM_ERR_TIMEOUT (a kernel gave up on a bounded wait, or the
+ * prefill GEMM found its shared memory misaligned; its output is undefined
+ * and the handle's device state has been reset), or
  * QMM_ERR_CUDA (the stream reported an error). */
 int qmm_sync_status(qmm_t h, void* stream);
 

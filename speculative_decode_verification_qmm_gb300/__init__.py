@@ -21,7 +21,7 @@ from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_
 
 __all__ = [
     "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_greedy", "qmm_verify_host",
-    "qmm_verify_noalloc", "qmm_sync_status",
+    "qmm_verify_noalloc", "qmm_prefill", "qmm_prefill_workspace", "qmm_sync_status",
     "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
     "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
     "QmmError", "load",
@@ -123,6 +123,22 @@ def qmm_verify_noalloc(h, act, out, M: int, stream=None) -> None:
     (no allocation; calls that overlap on the GPU race)."""
     _check("qmm_verify_noalloc", load().qmm_verify_noalloc(h, _ptr(act), act.stride(0), _ptr(out),
                                                            out.stride(0), M, _stream_ptr(stream)))
+
+
+def qmm_prefill_workspace(h, M: int) -> int:
+    """Bytes of device workspace qmm_prefill needs for M rows."""
+    n = ctypes.c_int64(0)
+    _check("qmm_prefill_workspace", load().qmm_prefill_workspace(h, M, ctypes.byref(n)))
+    return n.value
+
+
+def qmm_prefill(h, act, out, M: int, workspace, stream=None) -> None:
+    """Prefill product on an FP8 handle: act CUDA bf16 [M, lda>=K], out CUDA
+    fp32 [M, ldo>=N], workspace a CUDA tensor of at least
+    qmm_prefill_workspace(h, M) bytes; asynchronous."""
+    _check("qmm_prefill", load().qmm_prefill(
+        h, _ptr(act), act.stride(0), _ptr(out), out.stride(0), M, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
 
 
 def qmm_sync_status(h, stream=None) -> int:
@@ -278,6 +294,21 @@ class Matrix:
         accept = torch.empty(2, dtype=torch.int32, device=act.device)
         qmm_verify_greedy(self.handle, act, out, M, tokens, argmax, accept, stream)
         return out, argmax, accept
+
+    def prefill(self, act, out=None, stream=None):
+        """out[M, N] = act[M, K] W^T for any M (FP8 handles); the workspace is
+        kept on the Matrix and grown when a call needs more."""
+        import torch
+        M = act.shape[0]
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.float32, device=act.device)
+        need = qmm_prefill_workspace(self.handle, M)
+        ws = getattr(self, "_prefill_ws", None)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=act.device)
+            self._prefill_ws = ws
+        qmm_prefill(self.handle, act, out, M, ws, stream)
+        return out
 
     def info(self) -> dict:
         return qmm_get_info(self.handle)

@@ -78,6 +78,8 @@ SIGNATURES = {
     "qmm_verify_greedy": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P, _P, _P, _P]),
     "qmm_verify_host": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
     "qmm_verify_noalloc": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
+    "qmm_prefill": (_INT, [_P, _P, _I64, _P, _I64, _I64, _P, _I64, _P]),
+    "qmm_prefill_workspace": (_INT, [_P, _I64, ctypes.POINTER(_I64)]),
     "qmm_sync_status": (_INT, [_P, _P]),
     "qmm_last_cuda_error": (_INT, [_P]),
     "qmm_get_info": (_INT, [_P, ctypes.POINTER(qmm_info)]),

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libqmm.so")
 
 SOURCES = ["qmm_api.cu", "qmm_aux.cu", "qmm_verify_q4.cu", "qmm_verify_fp8.cu", "qmm_verify_q8.cu",
-           "qmm_verify_tc.cu"]
+           "qmm_verify_tc.cu", "qmm_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

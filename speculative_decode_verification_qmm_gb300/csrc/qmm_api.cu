@@ -311,6 +311,34 @@ cudaError_t act_map_for(qmm_handle* h, const void* rows, int64_t lda, int M, boo
   return cudaSuccess;
 }
 
+// The tensor map over the prefill pre-pass's f16 rows [M][K]: 2-D, boxes of
+// 64 columns x prefill_tile_rows() rows, 128-byte swizzle.
+cudaError_t prefill_map_for(qmm_handle* h, const void* rows, int M, const CUtensorMap** out) {
+  const int box_r = prefill_tile_rows(), box_k = 64;
+  for (auto& m : h->maps)
+    if (m.ptr == rows && m.lda == h->K && m.M == M && m.f16 && m.box_r == box_r && m.box_k == box_k) {
+      *out = &m.map;
+      return cudaSuccess;
+    }
+  qmm_handle::MapEntry& m = h->maps[h->map_next];
+  h->map_next = (h->map_next + 1) % qmm_handle::MAP_CACHE;
+  m.ptr = nullptr;
+  cudaError_t e = encode_act_map_2d(&m.map, rows, h->K, M, h->K, true, box_r, box_k);
+  if (e != cudaSuccess) return e;
+  m.ptr = rows;
+  m.lda = h->K;
+  m.M = M;
+  m.f16 = true;
+  m.box_r = box_r;
+  m.box_k = box_k;
+  *out = &m.map;
+  return cudaSuccess;
+}
+
+// Prefill workspace: f16 rows [M][K], then the rows' multipliers [M] fp32.
+int64_t prefill_rows_bytes(const qmm_handle* h, int64_t M) { return (M * h->K * 2 + 255) & ~(int64_t)255; }
+int64_t prefill_ws_bytes(const qmm_handle* h, int64_t M) { return prefill_rows_bytes(h, M) + M * 4; }
+
 // The verify kernel of the handle's plan, reading M activation rows of 16-bit
 // values at `rows` (the caller's bf16 rows, or the pre-pass's f16 scratch).
 cudaError_t launch_verify_kernel(qmm_handle* h, const VerifyParams& vp, const VerifyLaunch& vl,
@@ -389,6 +417,7 @@ int qmm_create(qmm_t* out, const qmm_desc* d, void* stream) {
   cudaError_t e = tc ? prepare_tc_attributes()
                      : (fmt == 0 ? prepare_q4_attributes()
                                  : (fmt == 2 ? prepare_q8_attributes() : prepare_fp8_attributes()));
+  if (e == cudaSuccess && fmt == 1) e = prepare_prefill_attributes();
   if (e != cudaSuccess) {
     free_handle(h);
     return cuda_fail(nullptr, e);
@@ -586,6 +615,54 @@ int qmm_verify_greedy(qmm_t h, const uint16_t* act, int64_t lda, float* out, int
                       const int32_t* tokens, int32_t* argmax, int32_t* accept, void* stream) {
   GreedyArgs g{tokens, argmax, accept};
   return verify_impl(h, act, lda, out, ldo, M, stream, &g);
+}
+
+int qmm_prefill_workspace(qmm_t h, int64_t M, int64_t* bytes) {
+  if (!bytes) return QMM_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (h->fmt != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
+  if (M < 1 || M > QMM_PREFILL_MAX_M) return QMM_ERR_M_RANGE;
+  *bytes = prefill_ws_bytes(h, M);
+  return QMM_OK;
+}
+
+int qmm_prefill(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int64_t M,
+                void* workspace, int64_t workspace_bytes, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (h->fmt != QMM_FMT_FP8_E4M3_B128) return QMM_ERR_INVALID_ARG;
+  if (M < 1 || M > QMM_PREFILL_MAX_M) return QMM_ERR_M_RANGE;
+  if (!act || !out || !workspace) return QMM_ERR_INVALID_ARG;
+  if (workspace_bytes < prefill_ws_bytes(h, M)) return QMM_ERR_INVALID_ARG;
+  if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 255) || lda < h->K ||
+      (lda & 7) || ldo < h->N)
+    return QMM_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint16_t* rows = static_cast<uint16_t*>(workspace);
+  float* row_scale = reinterpret_cast<float*>(static_cast<char*>(workspace) + prefill_rows_bytes(h, M));
+  cudaError_t e = launch_prefill_prep(act, lda, rows, row_scale, M, h->K, rotation_block(h->flags), st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  const CUtensorMap* map = nullptr;
+  e = prefill_map_for(h, rows, (int)M, &map);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  PrefillLaunch pl;
+  pl.wdev = h->wdev;
+  pl.f8_scale = h->f8_scale;
+  pl.row_scale = row_scale;
+  pl.out = out;
+  pl.status = h->status;
+  pl.ldo = ldo;
+  pl.M = (int)M;
+  pl.n_tiles = h->plan.n_tiles;
+  pl.spt = h->plan.S * h->plan.spc;
+  pl.kb_count = (int)(h->K / 128);
+  pl.sm_count = h->sm_count;
+  pl.wait_limit_ns = h->wait_limit_ns;
+  e = launch_prefill_fp8(pl, map, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return QMM_OK;
 }
 
 int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_host, int64_t ldo,

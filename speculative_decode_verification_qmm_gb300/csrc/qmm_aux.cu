@@ -9,49 +9,6 @@
 namespace qmm {
 
 // ---------------------------------------------------------------------------
-// B-point Walsh-Hadamard rotation (B = 32, 64 or 128) across B/4 lanes holding
-// 4 consecutive values each: strides 1 and 2 inside the lane, then strides
-// 4, 8, ..., B/2 with lane shuffles (partner lane = lane ^ 1, ^ 2, ..., ^ B/8).
-// Every stage maps the pair (x at the lower index, y at the upper) to
-// (x + y, x - y) in fp32, the stage order and arithmetic of the unnormalised
-// transform ["Qwen3.8-27B at 45.7 tok/s: DFlash2 in 1bit serve, and 4-bit
-// activations with a Hadamard rotation", section "Prompt processing: 4-bit
-// activations, rotated first": two in-register butterfly steps and three lane
-// shuffles for B = 32; the larger rotations that the page names as the next
-// step keep the stride-ascending order].  All 32 lanes of the warp must call
-// it (a warp holds 128 values: 128 / B blocks).
-// ---------------------------------------------------------------------------
-template <int B>
-__device__ __forceinline__ void fwht_lanes(float (&v)[4], int lane) {
-  static_assert(B == 32 || B == 64 || B == 128, "rotation size");
-  float x, y;
-  // stride 1: (0,1), (2,3)
-  x = v[0]; y = v[1]; v[0] = __fadd_rn(x, y); v[1] = __fsub_rn(x, y);
-  x = v[2]; y = v[3]; v[2] = __fadd_rn(x, y); v[3] = __fsub_rn(x, y);
-  // stride 2: (0,2), (1,3)
-  x = v[0]; y = v[2]; v[0] = __fadd_rn(x, y); v[2] = __fsub_rn(x, y);
-  x = v[1]; y = v[3]; v[1] = __fadd_rn(x, y); v[3] = __fsub_rn(x, y);
-  // strides 4 .. B/2 across lanes
-#pragma unroll
-  for (int d = 1; d < B / 4; d <<= 1) {
-    const bool upper = (lane & d) != 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float other = __shfl_xor_sync(0xFFFFFFFFu, v[e], d);
-      v[e] = upper ? __fsub_rn(other, v[e]) : __fadd_rn(v[e], other);
-    }
-  }
-}
-
-__device__ __forceinline__ void load4_bf16(const uint16_t* p, float (&v)[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(p);
-  v[0] = __uint_as_float((raw.x & 0xFFFFu) << 16);
-  v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-  v[2] = __uint_as_float((raw.y & 0xFFFFu) << 16);
-  v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-}
-
-// ---------------------------------------------------------------------------
 // Activation pre-pass.  CTA (s, m) converts row m's K range of split s into the
 // stage-ordered 16-bit scratch read by the verify kernel.
 //   OUT_F16 = false: bf16 copied unchanged (exact); multiplier 1.
@@ -414,10 +371,7 @@ __global__ void dequant_fp8_kernel(const uint8_t* __restrict__ wdev, const float
       const int64_t k = kbase + 16 * j + 2 * t + (e & 1) + 8 * (a >> 1);
       if (n < N && k < K) {
         const uint32_t code = (words[v] >> (8 * e)) & 0xFFu;
-        uint32_t h2;
-        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-            : "=r"(h2)
-            : "r"(code));
+        const uint32_t h2 = e4m3x2_to_f16x2(code);
         const float w = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
         out[n * K + k] = __fmul_rn(w, s);
       }

@@ -69,4 +69,29 @@ cudaError_t launch_quantize_q8(const float* w, int64_t N, int64_t K, uint8_t* bl
 cudaError_t launch_quantize_fp8(const float* w, int64_t N, int64_t K, int had, uint8_t* codes,
                                 float* scales, cudaStream_t st);
 
+// Prefill GEMM (FP8 handles): out[M][N] = act[M][K] * W^T for any M, on the
+// verify layout's stage stream.  act_map points to a CUtensorMap over the
+// pre-pass's f16 rows (2-D, boxes of 64 columns x prefill_tile_rows() rows,
+// 128-byte swizzle).
+struct PrefillLaunch {
+  const uint8_t* wdev;
+  const float* f8_scale;
+  const float* row_scale;
+  float* out;
+  int* status;
+  int64_t ldo;
+  int M;
+  int n_tiles;
+  int spt;       // stages per weight tile in the stream (S * spc)
+  int kb_count;  // K / 128
+  int sm_count;
+  uint64_t wait_limit_ns;
+};
+cudaError_t prepare_prefill_attributes();
+int prefill_tile_rows();
+// bf16 rows -> f16 rows times 2^e (row_scale[m] = 2^-e), rotated in hb-blocks when hb != 0.
+cudaError_t launch_prefill_prep(const uint16_t* act, int64_t lda, uint16_t* out, float* row_scale, int64_t M,
+                                int64_t K, int hb, cudaStream_t st);
+cudaError_t launch_prefill_fp8(const PrefillLaunch& pl, const void* act_map, cudaStream_t st);
+
 }  // namespace qmm

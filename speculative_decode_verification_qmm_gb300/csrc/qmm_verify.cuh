@@ -95,15 +95,6 @@ struct SmemLayout {
   static_assert(F::CHUNK_BYTES % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
 };
 
-// e4m3 pair (16 bits) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(v16));
-  return r;
-}
-
 // Shared-memory address of the 8 values k = 8 kc .. 8 kc + 7 of activation
 // row `row` in a chunk box: rows of RB = 2 x CHUNK_K bytes, and the tensor
 // map's RB-byte swizzle moves 16-byte piece kc of row r to kc ^ (r & 7)
