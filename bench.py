@@ -14,7 +14,9 @@ Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h
 q8_mlp, q8_attn (Q8_0 at the FP8 MLP and the attention shapes),
 fp8_mlp, model (64 layers x {qkv, out, gate+up, down}), q4_lmhead (the
 151,936 x 5120 output head through qmm_verify_greedy: the verify product plus
-the argmax and accepted-prefix step).
+the argmax and accepted-prefix step), fp8_prefill (the prompt-shaped FP8 GEMM,
+qmm_prefill, at M = 512 / 2048 / 8192 rows on the FP8 MLP weights; its own
+metric, TFLOP/s against the dense f16/bf16 tensor peak).
 
 Multi-GPU (--gpus N under torchrun): the path shards into independent
 problems, so every rank runs its own replica of the workload with no
@@ -522,6 +524,188 @@ def run_gpu(args, ws, rank, local):
     return line, rank
 
 
+# ---------------------------------------------------------------- prefill GEMM
+PREFILL_METRIC = "prefill FP8 GEMM TFLOP/s (% of GB300 dense bf16/f16 peak) at M=512/2048/8192 prompt rows"
+PREFILL_MS = (512, 2048, 8192)
+
+
+def measured_peak_tflops():
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, ws, rank, local):
+    """The prefill-shaped block-scaled FP8 GEMM (qmm_prefill) on the FP8 MLP
+    weights (N = 17408, K = 5120): one step = one call at each M of
+    PREFILL_MS.  Every timed call is preceded by an L2 flush (a 2 x L2 buffer
+    written between the events), so each call reads its operands from HBM."""
+    import torch
+    import speculative_decode_verification_qmm_gb300 as q
+    from speculative_decode_verification_qmm_gb300 import synth
+
+    torch.cuda.set_device(local)
+    q.load()
+    dev = torch.device("cuda", local)
+    spec = synth.SHAPES["fp8_mlp"]
+    N, K = spec["N"], spec["K"]
+    w = synth.weights_cuda(N, K, spec["seed"])
+    codes, scales = q.quantize_fp8(w)
+    del w
+    mat = q.Matrix(q.QMM_FMT_FP8_E4M3_B128, codes, N, K, scales=scales)
+    del codes, scales
+    Ms = PREFILL_MS
+    acts = {M: synth.activations_cuda(M, K, spec["seed"] + 1000 + M, outliers=True) for M in Ms}
+    outs = {M: torch.empty((M, N), dtype=torch.float32, device=dev) for M in Ms}
+    ws_bytes = max(q.qmm_prefill_workspace(mat.handle, M) for M in Ms)
+    wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(M, act=None, out=None):
+        q.qmm_prefill(mat.handle, acts[M] if act is None else act, outs[M] if out is None else out,
+                      M, wsbuf)
+
+    clocks = ClockSampler(local).__enter__()
+    time.sleep(0.5)
+    for _ in range(args.warmup):
+        for M in Ms:
+            call(M)
+    torch.cuda.synchronize()
+    if mat.sync_status() != q.QMM_OK:
+        raise RuntimeError("device status after warmup")
+    barrier(ws)
+    torch.cuda.synchronize()
+    n_before = len(clocks.lines)
+    marks = []
+    for _ in range(args.steps):
+        for M in Ms:
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(M)
+            b.record(stream)
+            marks.append((M, a, b))
+    torch.cuda.synchronize()
+    time.sleep(0.25)
+    clocks.__exit__(None, None, None)
+    clocks.lines = clocks.lines[max(0, n_before - 2):]
+    barrier(ws)
+    if mat.sync_status() != q.QMM_OK:
+        raise RuntimeError("device status after timing")
+    per_m = {M: [] for M in Ms}
+    for M, a, b in marks:
+        per_m[M].append(a.elapsed_time(b))
+    step_ms = sum(sum(v) for v in per_m.values()) / args.steps
+    step_ms = max_over_ranks(step_ms, ws, dev)
+    flops_per_step = sum(2.0 * M * N * K for M in Ms)
+    total_flops = sum_over_ranks(flops_per_step * args.steps, ws, dev)
+    value = total_flops / (step_ms * args.steps * 1e-3) / 1e12
+    peak, peak_kind = measured_peak_tflops()
+    breakdown = {}
+    for M in Ms:
+        xs = sorted(per_m[M])
+        med = statistics.median(xs)
+        qt = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
+        breakdown[str(M)] = {"ms_median": round(med, 4), "ms_p10": round(qt(0.1), 4),
+                             "ms_p90": round(qt(0.9), 4),
+                             "TFLOPs_median": round(2.0 * M * N * K / (med * 1e-3) / 1e12, 1)}
+    # the dominant launch: the M = 8192 call (pre-pass + GEMM), events on its stream
+    big = Ms[-1]
+    big_ms = statistics.median(per_m[big])
+    achieved = 2.0 * big * N * K / (big_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = {M: acts[M].cpu().pin_memory() for M in Ms}
+        host_out = {M: torch.empty((M, N), dtype=torch.float32).pin_memory() for M in Ms}
+        h2d = sum(M * K * 2 for M in Ms)
+        d2h = sum(M * N * 4 for M in Ms)
+
+        def e2e_step():
+            for M in Ms:
+                acts[M].copy_(host_in[M], non_blocking=True)
+                call(M)
+                host_out[M].copy_(outs[M], non_blocking=True)
+            torch.cuda.synchronize()
+
+        e2e_steps = max(1, min(args.steps, 5))
+        e2e_step()
+        barrier(ws)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        el = max_over_ranks(time.perf_counter() - t0, ws, dev)
+        e2e = {"value": round(sum_over_ranks(flops_per_step * e2e_steps, ws, dev) / el / 1e12, 1),
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps,
+               "api": "qmm_prefill (device buffers): per step and M the bf16 rows are copied from "
+                      "pinned host memory, the call is launched, the fp32 result is copied back "
+                      "to pinned host memory; one synchronize per step"}
+    traffic = recorded_traffic("fp8_prefill")
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(value, 1),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded N(0,0.02) weights quantized to E4M3 with 128x128 fp32 scales on "
+                "the device, bf16 N(0,1) activations with 0.1% x20 outlier channels)",
+        "config": {"workload": f"FP8 E4M3 128x128 prefill GEMM K={K} N={N}, "
+                               f"M={'/'.join(map(str, Ms))}",
+                   "l2": "L2 flushed (2 x L2 buffer written) before every timed call",
+                   "parallelism": f"replicas x{ws}", "per_M": breakdown,
+                   "pct_of_peak": round(100 * value / ws / peak, 1)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_fp8_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (cuBLAS bf16 burst; f16 has the same "
+                                                "nominal dense rate)", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "algorithmic_flops_per_launch": 2.0 * big * N * K,
+                     "note": f"M = {big} call (activation pre-pass + GEMM), median CUDA-event "
+                             "duration after an L2 flush"},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": 2 * len(Ms) * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores, sample = prefill_oracle_rate(args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    mat.close()
+    return line, rank
+
+
+def prefill_oracle_rate(budget_s: float):
+    """The oracle's rate (TFLOP/s) on a bounded sample of the prefill workload:
+    256 prompt rows against 256 of the 17408 weight rows, K = 5120."""
+    import oracle as O
+    from speculative_decode_verification_qmm_gb300 import synth
+    spec = synth.SHAPES["fp8_mlp"]
+    K, rows_n, M = spec["K"], 256, 256
+    w = synth.weights(rows_n, K, spec["seed"])
+    codes, sc = O.fp8_quantize(w)
+    a = synth.activations(M, K, spec["seed"] + 1000, outliers=True)
+    flops, t_total, reps = 0.0, 0.0, 0
+    while t_total < budget_s or reps == 0:
+        t0 = time.perf_counter()
+        O.verify_rows(O.FMT_FP8, codes, sc, rows_n, K, a)
+        t_total += time.perf_counter() - t0
+        flops += 2.0 * M * rows_n * K
+        reps += 1
+    sample = (f"{M} prompt rows x {rows_n} of {spec['N']} weight rows x K={K}, {reps} pass(es), "
+              f"{t_total:.1f} s")
+    return flops / t_total / 1e12, O.num_threads(), sample
+
+
 # ---------------------------------------------------------------- CPU oracle arm
 def oracle_sample_rate(budget_s: float, workload: str):
     """Time the oracle on a bounded row sample of the workload at every M of the
@@ -573,6 +757,27 @@ def cpu_baseline(args):
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
+    if args.workload == "fp8_prefill":
+        for _ in range(args.warmup):
+            prefill_oracle_rate(0.0)
+        vals = []
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            v, cores, sample = prefill_oracle_rate(max(1.0, args.cpu_budget / max(1, args.steps)))
+            vals.append(v)
+        elapsed = time.perf_counter() - t0
+        value = statistics.median(vals)
+        return {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+                "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(elapsed / args.steps * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded, same recipe as the GPU arm)",
+                "config": {"workload": "fp8_prefill (CPU oracle on a bounded sample)",
+                           "parallelism": "host cores"},
+                "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     for _ in range(args.warmup):
         oracle_sample_rate(0.0, args.workload)
     vals = []
@@ -612,7 +817,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=sorted(list(WORKLOADS) + ["model"]), default="q4_attn")
+    ap.add_argument("--workload", choices=sorted(list(WORKLOADS) + ["model", "fp8_prefill"]),
+                    default="q4_attn")
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: >= 4x L2)")
     ap.add_argument("--splits", type=int, default=0, help="force the K split count (0: planner)")
     ap.add_argument("--kernel", choices=sorted(KERNEL_FLAGS), default="auto",
@@ -637,7 +843,10 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    line, rank = run_gpu(args, ws, rank, local)
+    if args.workload == "fp8_prefill":
+        line, rank = run_prefill(args, ws, rank, local)
+    else:
+        line, rank = run_gpu(args, ws, rank, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

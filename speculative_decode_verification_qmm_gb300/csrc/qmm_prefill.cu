@@ -32,9 +32,11 @@
 //               scale * partial into fp32 registers (packed FMAs); after the
 //               last stage of a tile it writes out[m][n] = sum * 2^-e(m),
 //               32 consecutive n per store.
-// The accumulator and the A operand are double-buffered in tensor memory
-// (columns 0-255 and 256-383 of a 512-column allocation), so the MMAs of one
-// stage overlap the conversion of the next and the promotion of the last.
+// Tensor memory (512 columns) holds two accumulators (columns 0-255) and four
+// A operands (256-511), so the MMAs of one stage overlap the conversion of the
+// next three and the promotion of the last.  The MMA stream is bound by the
+// copies: a stage lands ~2 us after it is requested, and the ring's four
+// 48 KB stages are held until their MMAs complete.
 // Every wait is bounded; on a timeout the CTA records it in the status word,
 // stops, drains its own copies and MMAs in flight and frees tensor memory.
 #include <cuda.h>
@@ -49,6 +51,8 @@ namespace qmm {
 constexpr int PF_BM = 128;  // activation rows per tile (the MMA's N)
 constexpr int PF_BK = 128;  // columns per stage: one scale column
 constexpr int PF_NS = 4;    // stages in the shared-memory ring
+constexpr int PF_NA = 4;    // f16 weight (A operand) buffers in tensor memory
+constexpr int PF_ND = 2;    // fp32 accumulators in tensor memory
 constexpr int PF_WARPS = 14;
 constexpr int PF_THREADS = PF_WARPS * 32;
 constexpr int PF_CV_WARP0 = 2, PF_CV_WARPS = 4;
@@ -57,15 +61,16 @@ static_assert(PF_CV_WARP0 + PF_CV_WARPS == PF_EP_WARP0 && PF_EP_WARP0 + PF_EP_WA
 constexpr int PF_ACT_BYTES = PF_BM * PF_BK * 2;  // 32 KB: two 64-column swizzled halves
 constexpr int PF_TMEM_COLS = 512;
 constexpr int PF_D_COL = 0;    // accumulator b: columns b * 128 + [0, 128)
-constexpr int PF_A_COL = 256;  // A operand b: columns 256 + b * 64 + [0, 64)
+constexpr int PF_A_COL = PF_ND * PF_BM;  // A operand a: columns PF_A_COL + a * 64 + [0, 64)
+static_assert(PF_A_COL + PF_NA * (PF_BK / 2) <= PF_TMEM_COLS, "tensor memory budget");
 constexpr int PF_GROUP = 16;   // weight tiles per raster group
 
 struct PfSmem {
   static constexpr int ACT_OFF = 0;
   static constexpr int W_OFF = ACT_OFF + PF_NS * PF_ACT_BYTES;
   static constexpr int BAR_OFF = W_OFF + PF_NS * F8_STAGE_BYTES;
-  // full[NS], empty[NS], afull[2], aempty[2], dfull[2], dempty[2]
-  static constexpr int SLOT_OFF = BAR_OFF + (2 * PF_NS + 8) * 8;
+  // full[NS], empty[NS], afull[NA], aempty[NA], dfull[ND], dempty[ND]
+  static constexpr int SLOT_OFF = BAR_OFF + (2 * PF_NS + 2 * PF_NA + 2 * PF_ND) * 8;
   static constexpr int FLAG_OFF = SLOT_OFF + 16;
   static constexpr int BYTES = FLAG_OFF + 16;
   static_assert(PF_ACT_BYTES % 1024 == 0 && W_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -118,9 +123,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const uint32_t s_full = s_base + L::BAR_OFF;
   const uint32_t s_empty = s_full + NS * 8;
   const uint32_t s_afull = s_empty + NS * 8;
-  const uint32_t s_aempty = s_afull + 16;
-  const uint32_t s_dfull = s_aempty + 16;
-  const uint32_t s_dempty = s_dfull + 16;
+  const uint32_t s_aempty = s_afull + PF_NA * 8;
+  const uint32_t s_dfull = s_aempty + PF_NA * 8;
+  const uint32_t s_dempty = s_dfull + PF_ND * 8;
   // [0] abort, [1] stages committed by the MMA thread, [2] stages issued by the producer
   volatile int* s_flag = reinterpret_cast<volatile int*>(smem + L::FLAG_OFF);
 
@@ -129,9 +134,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(s_full + 8 * i, 1);
       mbar_init(s_empty + 8 * i, PF_CV_WARPS + 1);  // the converters and the MMA commit
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_afull + 8 * b, PF_CV_WARPS);
-      mbar_init(s_aempty + 8 * b, 1);
+    for (int a = 0; a < PF_NA; ++a) {
+      mbar_init(s_afull + 8 * a, PF_CV_WARPS);
+      mbar_init(s_aempty + 8 * a, 1);
+    }
+    for (int b = 0; b < PF_ND; ++b) {
       mbar_init(s_dfull + 8 * b, 1);
       mbar_init(s_dempty + 8 * b, PF_EP_WARPS);
     }
@@ -196,10 +203,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       bool ok = s_flag[0] == 0;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < kbs; ++kb) {
-          const int slot = u % NS, b = u & 1;
+          const int slot = u % NS, b = u % PF_ND, a = u % PF_NA;
           if (!mbar_wait_bounded(s_full + 8 * slot, (u / NS) & 1, lim) ||
-              !mbar_wait_bounded(s_afull + 8 * b, (u >> 1) & 1, lim) ||
-              (u >= 2 && !mbar_wait_bounded(s_dempty + 8 * b, ((u >> 1) - 1) & 1, lim))) {
+              !mbar_wait_bounded(s_afull + 8 * a, (u / PF_NA) & 1, lim) ||
+              (u >= PF_ND && !mbar_wait_bounded(s_dempty + 8 * b, ((u / PF_ND) - 1) & 1, lim))) {
             fail(DEV_ERR_TIMEOUT_FULL);
             ok = false;
             break;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           tc_fence_after();
           const uint32_t act = s_act + slot * PF_ACT_BYTES;
           const uint32_t d_t = tmem + PF_D_COL + b * PF_BM;
-          const uint32_t a_t = tmem + PF_A_COL + b * (PF_BK / 2);
+          const uint32_t a_t = tmem + PF_A_COL + a * (PF_BK / 2);
 #pragma unroll
           for (int kk = 0; kk < PF_BK / 16; ++kk) {
             const uint64_t bdesc =
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             tc_mma(d_t, a_t + kk * 8, bdesc, IDESC, kk > 0 ? 1u : 0u);
           }
           tc_commit(s_empty + 8 * slot);
-          tc_commit(s_aempty + 8 * b);
+          tc_commit(s_aempty + 8 * a);
           tc_commit(s_dfull + 8 * b);
           ++u;
           s_flag[1] = u;
@@ -233,9 +240,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     bool ok = __all_sync(0xFFFFFFFFu, s_flag[0] == 0);
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
       for (int kb = 0; kb < kbs; ++kb) {
-        const int slot = u % NS, b = u & 1;
+        const int slot = u % NS, a = u % PF_NA;
         if (!warp_wait(s_full + 8 * slot, (u / NS) & 1, lim) ||
-            (u >= 2 && !warp_wait(s_aempty + 8 * b, ((u >> 1) - 1) & 1, lim))) {
+            (u >= PF_NA && !warp_wait(s_aempty + 8 * a, ((u / PF_NA) - 1) & 1, lim))) {
           if (lane == 0) fail(DEV_ERR_TIMEOUT_FULL);
           ok = false;
           break;
@@ -264,13 +271,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
               r[2 * (4 * c + v) + 1] = e4m3x2_to_f16x2(w4[v] >> 16);
             }
           }
-          tmem_st_16x128b_x16(tmem + ((uint32_t)(32 * q + 16 * h) << 16) + PF_A_COL + b * (PF_BK / 2), r);
+          tmem_st_16x128b_x16(tmem + ((uint32_t)(32 * q + 16 * h) << 16) + PF_A_COL + a * (PF_BK / 2), r);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(s_afull + 8 * b);
+          mbar_arrive(s_afull + 8 * a);
           mbar_arrive(s_empty + 8 * slot);
         }
         ++u;
@@ -290,9 +297,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       for (int j = 0; j < 64; ++j) acc[j] = 0.f;
       const float* wsc = p.f8_scale + (size_t)nt * p.spt;
       for (int kb = 0; kb < kbs; ++kb) {
-        const int b = u & 1;
+        const int b = u % PF_ND;
         const float s = __ldg(wsc + kb);
-        if (!warp_wait(s_dfull + 8 * b, (u >> 1) & 1, lim)) {
+        if (!warp_wait(s_dfull + 8 * b, (u / PF_ND) & 1, lim)) {
           if (lane == 0) fail(DEV_ERR_TIMEOUT_FULL);
           ok = false;
           break;
@@ -337,7 +344,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     if (warp == 1 && lane == 0) {
       const int c = s_flag[1];
-      if (c > 0 && !mbar_wait_bounded(s_dfull + 8 * ((c - 1) & 1), ((c - 1) >> 1) & 1, 1000000000ull))
+      if (c > 0 &&
+          !mbar_wait_bounded(s_dfull + 8 * ((c - 1) % PF_ND), ((c - 1) / PF_ND) & 1, 1000000000ull))
         atomicOr(p.status, DEV_ERR_TIMEOUT_DRAIN);
     }
   }
