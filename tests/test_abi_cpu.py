@@ -84,6 +84,11 @@ def test_host_validation_without_device(L):
     assert L.qmm_get_info(None, None) == q.QMM_ERR_STATE
     assert L.qmm_dequantize(None, None, None) == q.QMM_ERR_STATE
     assert L.qmm_debug_set_wait_limit(None, 5) == q.QMM_ERR_STATE
+    # the prefill entry points answer on the handle first
+    n = ctypes.c_int64(7)
+    assert L.qmm_prefill(None, None, 0, None, 0, 64, None, 0, None) == q.QMM_ERR_STATE
+    assert L.qmm_prefill_workspace(None, 64, ctypes.byref(n)) == q.QMM_ERR_STATE and n.value == 0
+    assert L.qmm_prefill_workspace(None, 64, None) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_debug_fail_allocs(-1) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_debug_fail_allocs(0) == q.QMM_OK
     # a stale pointer that was never a live handle
