@@ -265,7 +265,8 @@ int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, in
  *         multipliers).
  * Asynchronous on `stream` (two kernels: the pre-pass and the GEMM).
  * Errors: STATE, INVALID_ARG (not an FP8 handle, NULL act/out/workspace,
- * workspace too small), M_RANGE, ALIGN, DEVICE, CUDA (launch). */
+ * workspace too small), M_RANGE, ALIGN, SHAPE (ceil(M/128) * N/128 * K/128,
+ * the GEMM's stage count, above 2^31 - 1), DEVICE, CUDA (launch). */
 #define QMM_PREFILL_MAX_M (1 << 22)
 int qmm_prefill(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int64_t M,
                 void* workspace, int64_t workspace_bytes, void* stream);

@@ -637,6 +637,9 @@ int qmm_prefill(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 255) || lda < h->K ||
       (lda & 7) || ldo < h->N)
     return QMM_ERR_ALIGN;
+  // the kernel counts tiles and 128-column stages in 32-bit integers
+  const int64_t pf_tiles = (int64_t)h->plan.n_tiles * ceil_div(M, prefill_tile_rows());
+  if (pf_tiles * (h->K / 128) > INT32_MAX) return QMM_ERR_SHAPE;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
   cudaStream_t st = (cudaStream_t)stream;
