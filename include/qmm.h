@@ -250,8 +250,9 @@ int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, in
  * 128 x 128-scaled E4M3 weights].  It reads the handle's weights as they are
  * (no second copy) and runs on the tcgen05 tensor cores: each activation row
  * (rotated first for the Hadamard flags) is scaled by a power of two 2^e that
- * brings its largest magnitude into [2^14, 2^15), rounded to f16 and written
- * to the workspace; the codes are converted to f16 exactly; every 128 x 128
+ * brings its largest magnitude into [2^14, 2^15), converted to f16 (exact for
+ * unrotated bf16 rows down to 2^-17 after scaling; the page's prefill also
+ * keeps 16-bit activations) and written to the workspace; the codes are converted to f16 exactly; every 128 x 128
  * tile product is accumulated in fp32, multiplied by its tile's scale and
  * added in fp32, and the row's sum is multiplied by 2^-e.  The result is held
  * to the same tolerance as qmm_verify.
