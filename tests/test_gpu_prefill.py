@@ -27,13 +27,13 @@ def _lib_built():
     torch.cuda.set_device(0)
 
 
-def fp8_matrix(N, K, seed, hadamard=False):
+def fp8_matrix(N, K, seed, hadamard=False, **kw):
     w = synth.weights(N, K, seed)
     if hadamard:
         w = O.rotate_weights_f32(w, 32 if hadamard is True else hadamard)
     codes, scales = O.fp8_quantize(w)
     mat = q.Matrix(q.QMM_FMT_FP8_E4M3_B128, torch.from_numpy(codes).cuda(), N, K,
-                   scales=torch.from_numpy(scales).cuda(), hadamard=hadamard)
+                   scales=torch.from_numpy(scales).cuda(), hadamard=hadamard, **kw)
     return mat, codes, scales
 
 
@@ -57,6 +57,36 @@ def test_prefill_fp8(N, K, M, hadamard):
     ref, S = O.verify_rows(O.FMT_FP8, codes, scales, N, K, a, hadamard=hadamard)
     assert_within_tolerance(out.cpu().double().numpy(), ref, S,
                             f"prefill N={N} K={K} M={M} H={hadamard}")
+    mat.close()
+
+
+def test_prefill_on_a_split_stream():
+    """A handle planned with 3 K splits stores 6 stages per weight tile for
+    K = 640 (5 stages of data, one of padding): the GEMM walks the 5."""
+    N, K, M = 256, 640, 150
+    mat, codes, scales = fp8_matrix(N, K, 960, k_splits=3)
+    info = mat.info()
+    assert info["k_splits"] * info["stages_per_cta"] > K // 128
+    a = synth.activations(M, K, 961, outliers=True)
+    out = mat.prefill(bf16_cuda(a))
+    torch.cuda.synchronize()
+    assert mat.sync_status() == q.QMM_OK
+    ref, S = O.verify_rows(O.FMT_FP8, codes, scales, N, K, a)
+    assert_within_tolerance(out.cpu().double().numpy(), ref, S, "prefill, split stream")
+    mat.close()
+
+
+def test_prefill_many_rows():
+    """70,000 prompt rows (547 activation tiles, a pre-pass of 8750 blocks)
+    against one weight tile, every output compared."""
+    N, K, M = 128, 256, 70_000
+    mat, codes, scales = fp8_matrix(N, K, 970)
+    a = synth.activations(M, K, 971, outliers=True)
+    out = mat.prefill(bf16_cuda(a))
+    torch.cuda.synchronize()
+    assert mat.sync_status() == q.QMM_OK
+    ref, S = O.verify_rows(O.FMT_FP8, codes, scales, N, K, a)
+    assert_within_tolerance(out.cpu().double().numpy(), ref, S, "prefill, 70k rows")
     mat.close()
 
 
