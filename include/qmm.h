@@ -42,6 +42,9 @@
  * stride-ascending stage order (strides 1, 2, ..., B/2) and weights divided by
  * B; at most one of the three is set.
  *
+ * qmm_prefill computes the same product for a prompt's worth of rows (any M)
+ * on an FP8 handle, as a tensor-core GEMM (see its comment below).
+ *
  * Conventions for every entry point:
  *   - Return value: QMM_OK (0) or one of the QMM_ERR_* codes below.  No call
  *     throws, aborts or prints.  qmm_strerror() names a code.
