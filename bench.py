@@ -440,8 +440,11 @@ def run_gpu(args, ws, rank, local):
 
     # ---- end to end through the public API: every step copies its
     # activations from pinned host memory to the device, makes its verify
-    # calls (qmm_verify, one per matrix and M, launched eagerly), copies all
-    # of its results back into pinned host memory, and waits for them.
+    # calls (qmm_verify, one per matrix and M), copies all of its results back
+    # into pinned host memory, and waits for them.  The calls run as the CUDA
+    # graphs captured above through the same API (an engine keeps its decode
+    # step in one graph); the same step with every call launched eagerly from
+    # Python is reported beside it.
     e2e = None
     if not args.no_e2e:
         plan = []  # per M: (device inputs, pinned host inputs, items, device outputs, pinned host outputs)
@@ -461,31 +464,43 @@ def run_gpu(args, ws, rank, local):
         h2d = sum(hi.numel() * 2 for ins, _, _, _ in plan for _, hi in ins)
         d2h = sum(ho.numel() * ho.element_size() for _, _, _, ho in plan)
 
-        def e2e_step():
-            for ins, items, dev_out, host_out in plan:
+        graph_of = {M: g for M, g, _ in graphs}
+
+        def e2e_step(graph_mode):
+            for (M, _), (ins, items, dev_out, host_out) in zip(groups, plan):
                 for d, hi in ins:
                     d.copy_(hi, non_blocking=True)
-                for j, (m, act, out) in enumerate(items):
-                    call(m, act, out, j)
+                if graph_mode:
+                    graph_of[M].replay()
+                else:
+                    for j, (m, act, out) in enumerate(items):
+                        call(m, act, out, j)
                 host_out.copy_(dev_out, non_blocking=True)
             torch.cuda.synchronize()
 
         e2e_steps = max(1, min(args.steps, 5))
-        e2e_step()  # warm
-        barrier(ws)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_step()
-        t1 = time.perf_counter()
-        el = max_over_ranks(t1 - t0, ws, dev)
+
+        def e2e_time(graph_mode):
+            e2e_step(graph_mode)  # warm
+            barrier(ws)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                e2e_step(graph_mode)
+            return max_over_ranks(time.perf_counter() - t0, ws, dev)
+
+        el = e2e_time(True)
+        el_eager = e2e_time(False)
         e2e_bytes = sum_over_ranks(bytes_per_step * e2e_steps, ws, dev)
         e2e = {"value": round(e2e_bytes / el / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps,
                "api": "qmm_verify (device buffers): per step the activations are copied from "
-                      "pinned host memory, every call is launched eagerly, all outputs are "
-                      "copied back to pinned host memory, then one synchronize"}
+                      "pinned host memory, the step's calls run as a CUDA graph captured through "
+                      "qmm_verify, all outputs are copied back to pinned host memory, then one "
+                      "synchronize",
+               "eager_value": round(e2e_bytes / el_eager / 1e9, 1),
+               "eager_api": "the same step with every qmm_verify call launched eagerly from Python"}
 
     traffic = recorded_traffic(args.workload)
     line = {
