@@ -2,9 +2,10 @@
 // act[M][K] * W[N][K]^T for any number of activation rows M, on the
 // 5th-generation tensor cores, with W the FP8 E4M3 codes of a verify handle
 // and one fp32 scale per 128 x 128 tile ["r9k: a from-scratch inference
-// engine for Qwen3.8-27B on two Radeon AI PRO R9700", introduction: the
+// engine for Qwen3.8-27B on two Radeon AI PRO R9700", opening section: the
 // prompt is processed by a block-scaled FP8 GEMM over weights in 128 x 128
-// scale blocks; section "What is next": block-scaled FP8 GEMMs for prefill].
+// scale blocks; its list of planned work names block-scaled FP8 GEMMs for
+// prefill again, and its correctness notes a BF16-activation prefill].
 //
 // Pre-pass (prefill_prep_kernel).  One warp per activation row: the row
 // (rotated in B-blocks for the Hadamard variants) is multiplied by 2^e, with e
