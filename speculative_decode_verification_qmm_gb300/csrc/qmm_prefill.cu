@@ -13,31 +13,32 @@
 // and written to the workspace; 2^-e is the row's output multiplier.
 //
 // GEMM (prefill_fp8_kernel), persistent, one CTA per SM.  A tile is 128
-// weight rows (one scale row) x 128 activation rows; tiles are visited in
+// weight rows (one scale row) x 192 activation rows; tiles are visited in
 // groups of 16 weight tiles, activation tiles fastest, so that the CTAs in
 // flight share both operands in L2.  Per 128-column stage (one scale column):
 //   warp 0      producer: one bulk copy of the stage's 16 KB of codes (the
 //               verify layout: units of 16 rows x 32 columns in mma.sync
 //               fragment order) and two 2-D tensor copies of the activation
-//               tile, 128 rows x 64 columns each, 128-byte swizzled;
+//               tile, 192 rows x 64 columns each, 128-byte swizzled;
 //   warp 1      allocates tensor memory; one thread issues eight
-//               tcgen05.mma (M = 128 weight rows, N = 128 activation rows,
+//               tcgen05.mma (M = 128 weight rows, N = 192 activation rows,
 //               K = 16; A = f16 weights in tensor memory, B = f16 activations
 //               in shared memory) into a fresh fp32 accumulator;
 //   warps 2-5   convert: warp q reads the units of rows 32q .. 32q + 31,
 //               converts E4M3 to f16 exactly (one cvt per pair) and stores
 //               them with tcgen05.st.16x128b, whose lane pattern is the
 //               fragment order of the units;
-//   warps 6-13  promote: warp (q, h) reads its 32 weight rows x 64 activation
-//               columns of the stage's accumulator (tcgen05.ld) and adds
-//               scale * partial into fp32 registers (packed FMAs); after the
-//               last stage of a tile it writes out[m][n] = sum * 2^-e(m),
-//               32 consecutive n per store.
-// Tensor memory (512 columns) holds two accumulators (columns 0-255) and four
-// A operands (256-511), so the MMAs of one stage overlap the conversion of the
-// next three and the promotion of the last.  The MMA stream is bound by the
-// copies: a stage lands ~2 us after it is requested, and the ring's four
-// 48 KB stages are held until their MMAs complete.
+//   warps 6-17  promote: warp (q, h) reads its 32 weight rows x 64 activation
+//               columns of the stage's accumulator (tcgen05.ld, 16 columns at
+//               a time) and adds scale * partial into fp32 registers (packed
+//               FMAs); after the last stage of a tile it writes
+//               out[m][n] = sum * 2^-e(m), 32 consecutive n per store.
+// Tensor memory (512 columns) holds two 192-column accumulators (columns
+// 0-383) and two A operands (384-511), so the MMAs of one stage overlap the
+// conversion of the next and the promotion of the last.  The ring's three
+// 64 KB stages are each held until their MMAs complete and a stage lands
+// ~2 us after it is requested, so the rate is set by the work per stage: the
+// widest activation tile the accumulators and the promotion registers allow.
 // Every wait is bounded; on a timeout the CTA records it in the status word,
 // stops, drains its own copies and MMAs in flight and frees tensor memory.
 #include <cuda.h>
@@ -49,19 +50,19 @@
 
 namespace qmm {
 
-constexpr int PF_BM = 128;  // activation rows per tile (the MMA's N)
+constexpr int PF_BM = 192;  // activation rows per tile (the MMA's N)
 constexpr int PF_BK = 128;  // columns per stage: one scale column
-constexpr int PF_NS = 4;    // stages in the shared-memory ring
-constexpr int PF_NA = 4;    // f16 weight (A operand) buffers in tensor memory
+constexpr int PF_NS = 3;    // stages in the shared-memory ring
+constexpr int PF_NA = 2;    // f16 weight (A operand) buffers in tensor memory
 constexpr int PF_ND = 2;    // fp32 accumulators in tensor memory
-constexpr int PF_WARPS = 14;
+constexpr int PF_WARPS = 18;
 constexpr int PF_THREADS = PF_WARPS * 32;
 constexpr int PF_CV_WARP0 = 2, PF_CV_WARPS = 4;
-constexpr int PF_EP_WARP0 = 6, PF_EP_WARPS = 8;
+constexpr int PF_EP_WARP0 = 6, PF_EP_WARPS = 12;  // 4 lane quarters x 3 column blocks
 static_assert(PF_CV_WARP0 + PF_CV_WARPS == PF_EP_WARP0 && PF_EP_WARP0 + PF_EP_WARPS == PF_WARPS, "warp roles");
-constexpr int PF_ACT_BYTES = PF_BM * PF_BK * 2;  // 32 KB: two 64-column swizzled halves
+constexpr int PF_ACT_BYTES = PF_BM * PF_BK * 2;  // 48 KB: two 64-column swizzled halves
 constexpr int PF_TMEM_COLS = 512;
-constexpr int PF_D_COL = 0;    // accumulator b: columns b * 128 + [0, 128)
+constexpr int PF_D_COL = 0;    // accumulator b: columns b * PF_BM + [0, PF_BM)
 constexpr int PF_A_COL = PF_ND * PF_BM;  // A operand a: columns PF_A_COL + a * 64 + [0, 64)
 static_assert(PF_A_COL + PF_NA * (PF_BK / 2) <= PF_TMEM_COLS, "tensor memory budget");
 constexpr int PF_GROUP = 16;   // weight tiles per raster group
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_fp8_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap amap) {
   using L = PfSmem;
   constexpr int NS = PF_NS;
-  constexpr uint32_t IDESC = tc_idesc_n(0u, PF_BM);  // f16 x f16 -> fp32, M = 128, N = 128
+  constexpr uint32_t IDESC = tc_idesc_n(0u, PF_BM);  // f16 x f16 -> fp32, M = 128, N = 192
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -306,14 +307,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           break;
         }
         tc_fence_after();
+        // 16 columns per load: 32 at a time spills the running sums at 18 warps
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld32(tmem + tl + PF_D_COL + b * PF_BM + h * 64 + half * 32, v);
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t v[16];
+          tmem_ld16(tmem + tl + PF_D_COL + b * PF_BM + h * 64 + qq * 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            ffma2(acc[half * 32 + j], acc[half * 32 + j + 1], s, __uint_as_float(v[j]),
+          for (int j = 0; j < 16; j += 2)
+            ffma2(acc[qq * 16 + j], acc[qq * 16 + j + 1], s, __uint_as_float(v[j]),
                   __uint_as_float(v[j + 1]));
         }
         tc_fence_before();
