@@ -38,7 +38,7 @@ __all__ = [
     "lib", "bf16_to_f64", "f16_to_f64", "e4m3_to_f64", "f32_to_f16_rne", "f32_to_e4m3_sat",
     "fwht32_f32", "fwht32_f64", "hadamard32_act_f32", "q4_0_quantize", "q4_0_quantize_h32",
     "fwht_f32", "fwht_f64", "hadamard_act_f32", "rotate_weights_f32",
-    "q4_0_dequant", "fp8_quantize", "fp8_dequant", "matmul_f64", "verify_rows",
+    "q4_0_dequant", "fp8_quantize", "fp8_dequant", "verify_rows",
     "num_threads", "set_num_threads", "FMT_Q4_0", "FMT_FP8", "FMT_Q8_0", "greedy_accept",
     "q8_0_quantize", "q8_0_dequant",
 ]
@@ -82,7 +82,6 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_q4_0_dequant.argtypes = [_P, _I64, _I64, _P]
     L.oracle_fp8_quantize.argtypes = [_P, _I64, _I64, _P, _P]
     L.oracle_fp8_dequant.argtypes = [_P, _P, _I64, _I64, _P]
-    L.oracle_matmul_f64.argtypes = [_P, _P, _INT, _I64, _I64, _P, _P]
     L.oracle_verify_rows.restype = _INT
     L.oracle_verify_rows.argtypes = [_INT, _P, _P, _I64, _I64, _P, _I64, _INT, _INT, _P,
                                      _I64, _P, _P]
@@ -290,19 +289,6 @@ def fp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- product
-def matmul_f64(act: np.ndarray, w: np.ndarray, want_s: bool = True):
-    """Naive triple loop: act [M][K] fp64, w [N][K] fp64 -> out [M][N] (and S)."""
-    a = _c(act, np.float64)
-    ww = _c(w, np.float64)
-    M, K = a.shape
-    N = ww.shape[0]
-    assert ww.shape[1] == K
-    out = np.empty((M, N), np.float64)
-    S = np.empty((M, N), np.float64) if want_s else None
-    lib().oracle_matmul_f64(_ptr(a), _ptr(ww), M, N, K, _ptr(out), _ptr(S) if want_s else None)
-    return (out, S) if want_s else out
-
-
 def _hb(hadamard) -> int:
     """Rotation block size from False / True (32) / 32 / 64 / 128."""
     if hadamard is True:

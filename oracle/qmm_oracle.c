@@ -420,24 +420,6 @@ void oracle_fp8_dequant(const uint8_t* codes, const float* scales, int64_t N, in
 /* The verify matmul: naive triple loop in fp64.                             */
 /* ------------------------------------------------------------------------ */
 
-/* act: [M][K] fp64, w: [N][K] fp64, out/S: [M][N] fp64 (S may be NULL). */
-void oracle_matmul_f64(const double* act, const double* w, int M, int64_t N, int64_t K,
-                       double* out, double* S) {
-#pragma omp parallel for schedule(static)
-  for (int64_t n = 0; n < N; ++n) {
-    for (int m = 0; m < M; ++m) {
-      double acc = 0.0, sabs = 0.0;
-      for (int64_t k = 0; k < K; ++k) {
-        double p = act[(int64_t)m * K + k] * w[n * K + k];
-        acc += p;
-        sabs += fabs(p);
-      }
-      out[(int64_t)m * N + n] = acc;
-      if (S) S[(int64_t)m * N + n] = sabs;
-    }
-  }
-}
-
 /* Decode the bf16 activation rows to fp64; in the Hadamard variants rotate
  * each B-block exactly in fp64 (sums of up to 128 bf16 values are exact in
  * fp64).  hadamard: 0 none, 1 or 32, 64, 128 = the block size B. */
@@ -531,14 +513,27 @@ void oracle_set_num_threads(int n) {
  * precisely": the batched target forward checks every drafted token against
  * the target's own greedy choice and commits the agreeing prefix].
  *   logits: [M][ld] fp64, row m = the target's scores over N tokens at block
- *           position m (finite values)
+ *           position m
  *   tokens: [M] the block's input tokens: tokens[0] is the last committed
  *           token, tokens[1..M-1] the drafted ones
- *   argmax: [M] out: the first index of the largest score of each row
+ *   argmax: [M] out: the first index of the largest score of each row, a
+ *           NaN counting as larger than every number (so the first NaN of a
+ *           row wins) and -0 as equal to +0.  The pages state the rule in
+ *           words only; this reading makes the argmax total, so that a
+ *           non-finite score cannot make the choice depend on the order
+ *           in which the scores are visited.
  *   result: [2] out: result[0] = k, the largest k <= M - 1 with
  *           argmax[m] == tokens[m + 1] for every m < k (the accepted drafts),
  *           and result[1] = argmax[k], the target's own token after them.
  * Returns 0, or -1 on bad sizes. */
+/* "x ranks above y" in the order the argmax uses: every NaN above every
+ * number and all NaNs equal to one another; -0 and +0 equal (plain >). */
+static int score_above(double x, double y) {
+  if (isnan(y)) return 0;
+  if (isnan(x)) return 1;
+  return x > y;
+}
+
 int oracle_greedy_accept(const double* logits, int64_t ld, int M, int64_t N,
                          const int32_t* tokens, int32_t* argmax, int32_t* result) {
   if (M <= 0 || N <= 0 || ld < N || N > 2147483647) return -1;
@@ -546,7 +541,7 @@ int oracle_greedy_accept(const double* logits, int64_t ld, int M, int64_t N,
     const double* row = logits + (int64_t)m * ld;
     int64_t best = 0;
     for (int64_t n = 1; n < N; ++n)
-      if (row[n] > row[best]) best = n;
+      if (score_above(row[n], row[best])) best = n;
     argmax[m] = (int32_t)best;
   }
   int k = 0;

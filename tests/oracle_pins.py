@@ -526,8 +526,8 @@ def check_greedy_golden(O):
 
 
 def check_greedy_vs_library(O):
-    """Argmax against numpy's (first occurrence of the maximum), on scores
-    rounded coarsely so that ties are frequent; k against a brute-force count
+    """Argmax against numpy's (first occurrence of the maximum, the first NaN
+    where there is one), on scores rounded coarsely so that ties are frequent; k against a brute-force count
     of the leading agreements, with drafts built to agree up to a chosen
     position."""
     rng = np.random.default_rng(11)
@@ -535,6 +535,12 @@ def check_greedy_vs_library(O):
         M = int(rng.integers(1, 17))
         N = int(rng.integers(1, 40))
         lg = np.round(rng.standard_normal((M, N)) * 2.0) / 2.0
+        if trial % 4 == 3:  # a few NaN scores: numpy's argmax returns the first NaN
+            lg[rng.random((M, N)) < 0.1] = np.nan
+        if trial % 8 == 5:  # signed zeros as the maximum: equal, the first one wins
+            lg = -np.abs(lg)
+            lg[rng.random((M, N)) < 0.3] = -0.0
+            lg[rng.random((M, N)) < 0.3] = 0.0
         ref = np.argmax(lg, axis=1).astype(np.int32)
         j = int(rng.integers(0, M))  # drafts agree at positions < j
         tokens = rng.integers(0, N, M).astype(np.int32)

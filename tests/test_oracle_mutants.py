@@ -58,8 +58,10 @@ MUTANTS = [
     ("q8_round_trunc", "int qi = (int)roundf(x[j] * inv);", "int qi = (int)(x[j] * inv);", None),
     ("q8_drops_sign_of_d", "(uint16_t)(blk[0] | (blk[1] << 8)));\n    for (int j = 0; j < 32; ++j) row",
      "(uint16_t)(blk[0] | ((blk[1] & 0x7F) << 8)));\n    for (int j = 0; j < 32; ++j) row", None),
-    ("greedy_last_tie", "if (row[n] > row[best]) best = n;", "if (row[n] >= row[best]) best = n;", None),
-    ("greedy_argmin", "if (row[n] > row[best]) best = n;", "if (row[n] < row[best]) best = n;", None),
+    ("greedy_last_tie", "  return x > y;\n}", "  return x >= y;\n}", None),
+    ("greedy_argmin", "  return x > y;\n}", "  return x < y;\n}", None),
+    ("greedy_nan_ignored", "if (score_above(row[n], row[best])) best = n;", "if (row[n] > row[best]) best = n;", None),
+    ("greedy_last_nan", "  if (isnan(y)) return 0;\n", "", None),
     ("greedy_token_offset", "argmax[k] == tokens[k + 1]", "argmax[k] == tokens[k]", None),
     ("greedy_k_short", "while (k < M - 1 && argmax", "while (k < M - 2 && argmax", None),
     ("greedy_next_is_last_draft", "result[1] = argmax[k];", "result[1] = argmax[k > 0 ? k - 1 : 0];", None),
