@@ -221,24 +221,25 @@ int qmm_verify_host(qmm_t h, const uint16_t* act_host, int64_t lda, float* out_h
  * CUDA graph under the global capture mode (cudaMalloc is refused there), or a
  * host runtime that owns every device allocation and hands the library only
  * the buffers it passes.  This call allocates nothing and does not use the
- * working memory of the handle: on the paths that need working memory (the
- * Hadamard rotation and FP8, whose activations go through the pre-pass) the
- * rotated activation rows and their per-(row, split) factors live in one fixed
- * array of QMM_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
- * that loads the library holds until the process exits; the bf16 Q4_0 path
- * reads the caller's rows directly and needs none.  The handle (created
- * earlier, which does allocate) supplies the weights and the status word; act
- * and out follow qmm_verify's rules.
+ * working memory of the handle: the rotated or f16 activation rows and their
+ * per-(row, split) factors (the Hadamard and FP8 / Q8_0 paths), the split-K
+ * partials and the per-tile arrival counts (plans with more than one K split)
+ * live in one fixed array of QMM_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The handle (created earlier, which does allocate) supplies the
+ * weights and the status word; act and out follow qmm_verify's rules.
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream
  *     capture.
- *   - All calls share the array and it keeps the last call's contents; every
- *     call rewrites the part it reads before reading it.  Calls that overlap
- *     on the GPU (other streams, other threads) race on the array and give
- *     wrong results; serialise them.
+ *   - All calls share the array and it keeps the last call's contents.  Every
+ *     call rewrites the parts it reads before reading them, and clears the
+ *     arrival counts (which must start at zero) with an asynchronous memset on
+ *     `stream` first.  Calls that overlap on the GPU (other streams, other
+ *     threads) race on the array and give wrong results; serialise them.
  *   - Asynchronous on `stream`.
- * Errors: as qmm_verify, plus QMM_ERR_SHAPE when the handle's rotated or FP8
- * activations need more than the array holds (K above about 127,000). */
+ * Errors: as qmm_verify, plus QMM_ERR_SHAPE when the handle's plan needs more
+ * than the array holds (f16 activations for K above about 127,000 columns, or
+ * rows x splits beyond about 500 row tiles x K splits). */
 #define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
 int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo,
                        int M, void* stream);

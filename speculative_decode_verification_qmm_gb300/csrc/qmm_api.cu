@@ -524,19 +524,42 @@ struct GreedyArgs {
   int32_t* accept;
 };
 
-// qmm_verify, and qmm_verify_greedy when `g` is not NULL.
-int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
-                void* stream, const GreedyArgs* g) {
+// The working memory of one verify call: the pre-pass's f16 rows and their
+// per-(row, split) factors (f16 paths only), the split-K partials and the
+// per-tile arrival counts (S > 1 only; the counts are zero on entry).
+struct VerifyScratch {
+  uint16_t* act = nullptr;
+  float* out_scale = nullptr;
+  float* ws = nullptr;
+  int* counters = nullptr;
+};
+
+VerifyScratch handle_scratch(const qmm_handle* h) {
+  VerifyScratch sc;
+  sc.act = h->act_scratch;
+  sc.out_scale = h->out_scale;
+  sc.ws = h->ws;
+  sc.counters = h->counters;
+  return sc;
+}
+
+// Argument checks shared by every verify entry point.
+int check_verify_args(qmm_t h, const uint16_t* act, int64_t lda, const float* out, int64_t ldo,
+                      int M) {
   if (!is_live(h)) return QMM_ERR_STATE;
   if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
   if (!act || !out) return QMM_ERR_INVALID_ARG;
-  if (g && (!g->tokens || !g->argmax || !g->accept || h->plan.tc)) return QMM_ERR_INVALID_ARG;
-  if (g && (((uintptr_t)g->tokens | (uintptr_t)g->argmax | (uintptr_t)g->accept) & 3))
-    return QMM_ERR_ALIGN;
   if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || lda < h->K || (lda & 7) || ldo < h->N)
     return QMM_ERR_ALIGN;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  return QMM_OK;
+}
+
+// qmm_verify, and qmm_verify_greedy when `g` is not NULL, with the working
+// memory `sc` (the handle's own, or the fixed array of qmm_verify_noalloc).
+int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
+                void* stream, const GreedyArgs* g, const VerifyScratch& sc) {
   cudaStream_t st = (cudaStream_t)stream;
   const Plan& p = h->plan;
   const int hb = rotation_block(h->flags);
@@ -549,9 +572,9 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
     PrepParams pp;
     pp.act = act;
     pp.lda = lda;
-    pp.out = h->act_scratch;
+    pp.out = sc.act;
     pp.ld_out = h->act_ld;
-    pp.out_scale = h->out_scale;
+    pp.out_scale = sc.out_scale;
     pp.K = h->K;
     pp.M = M;
     pp.S = p.S;
@@ -565,7 +588,7 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   vp.wdev = h->wdev;
   vp.f8_scale = h->f8_scale;
   vp.K = h->K;
-  vp.out_scale = f16 ? h->out_scale : nullptr;
+  vp.out_scale = f16 ? sc.out_scale : nullptr;
   vp.out = out;
   vp.status = h->status;
   vp.ldo = ldo;
@@ -573,8 +596,8 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   vp.M = M;
   vp.S = p.S;
   vp.spc = p.spc;
-  vp.ws = h->ws;
-  vp.counters = h->counters;
+  vp.ws = sc.ws;
+  vp.counters = sc.counters;
   vp.wait_limit_ns = h->wait_limit_ns;
   vp.best = nullptr;
   vp.tiles_done = nullptr;
@@ -595,12 +618,11 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
   vl.ctas = p.n_tiles * p.S;
   vl.stream = st;
-  e = f16 ? launch_verify_kernel(h, vp, vl, h->act_scratch, h->act_ld, M, true)
+  e = f16 ? launch_verify_kernel(h, vp, vl, sc.act, h->act_ld, M, true)
           : launch_verify_kernel(h, vp, vl, act, lda, M, false);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return QMM_OK;
 }
-
 
 }  // namespace
 
@@ -608,13 +630,21 @@ extern "C" {
 
 int qmm_verify(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
                void* stream) {
-  return verify_impl(h, act, lda, out, ldo, M, stream, nullptr);
+  const int rc = check_verify_args(h, act, lda, out, ldo, M);
+  if (rc != QMM_OK) return rc;
+  return verify_impl(h, act, lda, out, ldo, M, stream, nullptr, handle_scratch(h));
 }
 
 int qmm_verify_greedy(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t ldo, int M,
                       const int32_t* tokens, int32_t* argmax, int32_t* accept, void* stream) {
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
+  if (!tokens || !argmax || !accept || h->plan.tc) return QMM_ERR_INVALID_ARG;
+  if (((uintptr_t)tokens | (uintptr_t)argmax | (uintptr_t)accept) & 3) return QMM_ERR_ALIGN;
+  const int rc = check_verify_args(h, act, lda, out, ldo, M);
+  if (rc != QMM_OK) return rc;
   GreedyArgs g{tokens, argmax, accept};
-  return verify_impl(h, act, lda, out, ldo, M, stream, &g);
+  return verify_impl(h, act, lda, out, ldo, M, stream, &g, handle_scratch(h));
 }
 
 int qmm_prefill_workspace(qmm_t h, int64_t M, int64_t* bytes) {
@@ -700,9 +730,10 @@ int qmm_sync_status(qmm_t h, void* stream) {
   e = cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (word != 0) {
-    // A kernel gave up: clear the word so the handle can be used again.
-    cudaMemset(h->status, 0, sizeof(int));
-    e = cudaDeviceSynchronize();
+    // A kernel gave up: clear the word on the handle's stream so the handle
+    // can be used again (other streams of the device are not waited for).
+    e = cudaMemsetAsync(h->status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(h, e);
     return QMM_ERR_TIMEOUT;
   }
@@ -903,74 +934,43 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 extern "C" int qmm_verify_noalloc(qmm_t h, const uint16_t* act, int64_t lda, float* out,
                                   int64_t ldo, int M, void* stream) {
-  if (!is_live(h)) return QMM_ERR_STATE;
-  if (M < 1 || M > MAX_M) return QMM_ERR_M_RANGE;
-  if (!act || !out) return QMM_ERR_INVALID_ARG;
-  if (((uintptr_t)act & 15) || ((uintptr_t)out & 15) || lda < h->K || (lda & 7) || ldo < h->N)
-    return QMM_ERR_ALIGN;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return QMM_ERR_DEVICE;
+  const int rc = check_verify_args(h, act, lda, out, ldo, M);
+  if (rc != QMM_OK) return rc;
   const Plan& p = h->plan;
-  const int hb = rotation_block(h->flags);
-  const bool had = hb > 0;
-  const bool f16 = had || h->fmt != 0;
-  // Carve the array: activation scratch | per-(row, split) factors.  Both are
-  // written in full by the pre-pass before the verify kernel reads them, so
-  // nothing has to be cleared; the bf16 path reads the caller's rows and uses
-  // no working memory at all.
-  const size_t act_off = 0;
-  const size_t scale_off = align256(act_off + h->act_bytes);
-  const size_t total = scale_off + (size_t)MAX_M * p.S * sizeof(float);
-  if (f16 && total > STATIC_SCRATCH_BYTES) return QMM_ERR_SHAPE;
+  const bool f16 = rotation_block(h->flags) > 0 || h->fmt != 0;
+  // Carve the array: [f16 rows | per-(row, split) factors] on the f16 paths,
+  // then [split partials | per-tile arrival counts] when the plan splits K.
+  // The pre-pass writes the first two in full and the kernel writes every
+  // partial before it is read, so only the counts have to start at zero:
+  // they are cleared on the stream before the kernel runs.
+  size_t off = 0;
+  const size_t act_off = off;
+  if (f16) off = align256(off + h->act_bytes);
+  const size_t scale_off = off;
+  if (f16) off = align256(off + (size_t)MAX_M * p.S * sizeof(float));
+  const bool split = !p.tc && p.S > 1;
+  const size_t ws_off = off;
+  if (split) off = align256(off + (size_t)p.n_tiles * p.S * MAX_M * TILE_N * sizeof(float));
+  const size_t cnt_off = off;
+  if (split) off = align256(off + (size_t)p.n_tiles * sizeof(int));
+  if (off > STATIC_SCRATCH_BYTES) return QMM_ERR_SHAPE;
+  int dev = -1;
+  cudaGetDevice(&dev);
   unsigned char* base = nullptr;
   cudaError_t e = static_scratch_addr(dev, &base);
   if (e != cudaSuccess) return cuda_fail(h, e);
-  cudaStream_t st = (cudaStream_t)stream;
+  VerifyScratch sc;
   if (f16) {
-    PrepParams pp;
-    pp.act = act;
-    pp.lda = lda;
-    pp.out = reinterpret_cast<uint16_t*>(base + act_off);
-    pp.ld_out = h->act_ld;
-    pp.out_scale = reinterpret_cast<float*>(base + scale_off);
-    pp.K = h->K;
-    pp.M = M;
-    pp.S = p.S;
-    pp.spc = p.spc;
-    pp.stage_k = p.stage_k;
-    e = launch_act_prep(pp, f16, hb, st);
+    sc.act = reinterpret_cast<uint16_t*>(base + act_off);
+    sc.out_scale = reinterpret_cast<float*>(base + scale_off);
+  }
+  if (split) {
+    sc.ws = reinterpret_cast<float*>(base + ws_off);
+    sc.counters = reinterpret_cast<int*>(base + cnt_off);
+    e = cudaMemsetAsync(sc.counters, 0, (size_t)p.n_tiles * sizeof(int), (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
-
-  VerifyParams vp;
-  vp.wdev = h->wdev;
-  vp.f8_scale = h->f8_scale;
-  vp.K = h->K;
-  vp.out_scale = f16 ? reinterpret_cast<const float*>(base + scale_off) : nullptr;
-  vp.out = out;
-  vp.status = h->status;
-  vp.ldo = ldo;
-  vp.N = h->N;
-  vp.M = M;
-  vp.S = p.S;
-  vp.spc = p.spc;
-  vp.ws = h->ws;
-  vp.counters = h->counters;
-  vp.wait_limit_ns = h->wait_limit_ns;
-  vp.best = nullptr;
-  vp.tiles_done = nullptr;
-  vp.tokens = nullptr;
-  vp.argmax_out = nullptr;
-  vp.accept_out = nullptr;
-  vp.n_tiles = p.n_tiles;
-  VerifyLaunch vl;
-  vl.fmt = h->fmt;
-  vl.f16_ops = f16;
-  vl.simt = (h->flags & QMM_FLAG_SIMT) != 0;
-  vl.ctas = p.n_tiles * p.S;
-  vl.stream = st;
-  e = f16 ? launch_verify_kernel(h, vp, vl, base + act_off, h->act_ld, M, true)
-          : launch_verify_kernel(h, vp, vl, act, lda, M, false);
-  if (e != cudaSuccess) return cuda_fail(h, e);
-  return QMM_OK;
+  // (the tcgen05 kernel serves the bf16 path and reduces its splits inside a
+  // thread-block cluster: it needs none of the array)
+  return verify_impl(h, act, lda, out, ldo, M, stream, nullptr, sc);
 }

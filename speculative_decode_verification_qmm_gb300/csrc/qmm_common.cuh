@@ -310,19 +310,9 @@ struct Bf16Op {
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
           "f"(c[3]));
   }
-  // Offset form: 4 pairs of 128 + q (exact) from one 32-bit word of 8 nibbles,
-  // pair p from nibbles (p, p + 4), one lop3 per pair; the kernel adds
-  // -136 * sum(a) through the MMA's accumulator input instead of subtracting
-  // 136 from every weight.
-  __device__ __forceinline__ static void biased_word(uint32_t w, uint32_t (&r)[4]) {
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-      asm("lop3.b32 %0, %1, %2, %3, 0xEA;"
-          : "=r"(r[p])
-          : "r"(w >> (4 * p)), "r"(0x000F000Fu), "r"(0x43004300u));
-  }
-  // The same pairs as q - 8: bf16 128.0 = 0x4300 has a 7-bit mantissa whose
-  // low 4 bits take q exactly; subtracting 136 = 0x4308 leaves q - 8.
+  // 4 pairs of q - 8 from one 32-bit word of 8 nibbles, pair p from nibbles
+  // (p, p + 4): bf16 128.0 = 0x4300 has a 7-bit mantissa whose low 4 bits
+  // take q exactly (one lop3), and subtracting 136 = 0x4308 leaves q - 8.
   __device__ __forceinline__ static void dequant_word(uint32_t w, uint32_t (&r)[4]) {
     const uint32_t magic = 0x43004300u, bias = 0x43084308u;
 #pragma unroll

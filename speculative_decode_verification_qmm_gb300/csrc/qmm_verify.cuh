@@ -142,26 +142,11 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
   const int g = lane >> 2;
   uint32_t b[4][4];
   load_b_frags<4, 8 * NT8, 2 * Q4_STAGE_K / STAGE_CHUNKS>(abase, lane, b);
-  // bf16: the weights enter the MMA as 128 + q and every block's accumulator
-  // starts at -136 * sum_k a[m][k] (an MMA with a constant A operand), so the
-  // block sum is sum (q - 8) a without a subtraction per weight.  f16: the
-  // dequantizer returns q - 8 itself and the blocks start at zero.
-  constexpr bool FOLD = std::is_same<Op, Bf16Op>::value;
-  float c0[2][NT8][4];
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-    for (int j = 0; j < NT8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c0[blk][j][e] = 0.f;
-      if constexpr (FOLD) {
-        constexpr uint32_t kNeg136 = 0xC308C308u;  // bf16x2 (-136, -136)
-        Op::mma(c0[blk][j], kNeg136, kNeg136, kNeg136, kNeg136, b[2 * blk][2 * j],
-                b[2 * blk][2 * j + 1], c0[blk][j]);
-        Op::mma(c0[blk][j], kNeg136, kNeg136, kNeg136, kNeg136, b[2 * blk + 1][2 * j],
-                b[2 * blk + 1][2 * j + 1], c0[blk][j]);
-      }
-    }
+  // The weights enter the MMA as the exact values q - 8 (bf16 or f16), so a
+  // block's partial is the sum of exact products and never the difference of
+  // two large sums: a block of zero weights gives exactly zero whatever the
+  // activations are.
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int r = 0; r < WARP_SUBTILES; ++r) {
     const uint32_t unit = wunit0 + (uint32_t)(r * Q4_UNIT_BYTES);
@@ -171,20 +156,15 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       uint32_t a0[4], a1[4];
-      if constexpr (FOLD) {
-        Bf16Op::biased_word(words[2 * blk + 0], a0);
-        Bf16Op::biased_word(words[2 * blk + 1], a1);
-      } else {
-        Op::dequant_word(words[2 * blk + 0], a0);
-        Op::dequant_word(words[2 * blk + 1], a1);
-      }
+      Op::dequant_word(words[2 * blk + 0], a0);
+      Op::dequant_word(words[2 * blk + 1], a1);
       const uint32_t dpair = blk ? sc.y : sc.x;  // (d[g], d[g+8]) of this block
       const float dg = __half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF)));
       const float dg8 = __half2float(__ushort_as_half((unsigned short)(dpair >> 16)));
 #pragma unroll
       for (int j = 0; j < NT8; ++j) {
         float pp[4];
-        Op::mma(pp, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], c0[blk][j]);
+        Op::mma(pp, a0[0], a0[1], a0[2], a0[3], b[2 * blk][2 * j], b[2 * blk][2 * j + 1], zero);
         Op::mma(pp, a1[0], a1[1], a1[2], a1[3], b[2 * blk + 1][2 * j], b[2 * blk + 1][2 * j + 1], pp);
         ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
         ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);
@@ -193,50 +173,43 @@ __device__ __forceinline__ void q4_stage_mma(uint32_t wunit0, uint32_t abase, in
   }
 }
 
-// Q8_0 codes stored as u = q + 128, two bytes -> f16x2 (1024 + u, exact) by
-// one byte permute: result bytes (b_lo, 0x64, b_hi, 0x64).
-__device__ __forceinline__ uint32_t u8x2_to_f16x2_biased(uint32_t w, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0x64646464u), "r"(sel));
+// Q8_0 codes stored as u = q + 128, two bytes -> f16x2 (q, exact): one byte
+// permute gives (b_lo, 0x64, b_hi, 0x64) = 1024 + u = 1152 + q, and one packed
+// subtraction of 1152 leaves q (every integer below 2048 is an f16 value).
+__device__ __forceinline__ uint32_t u8x2_to_f16x2(uint32_t w, uint32_t sel) {
+  uint32_t x, r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(x) : "r"(w), "r"(0x64646464u), "r"(sel));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64806480u));
   return r;
 }
 
 // Q8_0: the chunk's 32 columns are one block per row.  The weights enter the
-// MMA as 1152 + q (f16, exact) and each block's accumulator starts at
-// -1152 * sum_k a[m][k] (an MMA with a constant A operand), so the block sum
-// is sum q a without a subtraction per weight; the block scale d (per row)
-// is then applied with packed fp32 FMAs, as for Q4_0.
+// MMA as the exact codes q (f16), so each block's partial is a sum of exact
+// products; the block scale d (per row) is then applied with packed fp32
+// FMAs, as for Q4_0.
 template <int NT8>
 __device__ __forceinline__ void q8_stage_mma(uint32_t wunit0, uint32_t abase, int lane,
                                              float (&acc)[WARP_SUBTILES][2][4]) {
   const int g = lane >> 2;
   uint32_t b[2][4];
   load_b_frags<2, 8 * NT8, 2 * Q8_STAGE_K / STAGE_CHUNKS>(abase, lane, b);
-  float c0[NT8][4];
-#pragma unroll
-  for (int j = 0; j < NT8; ++j) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) c0[j][e] = 0.f;
-    constexpr uint32_t kNeg1152 = 0xE480E480u;  // f16x2 (-1152, -1152)
-    F16Op::mma(c0[j], kNeg1152, kNeg1152, kNeg1152, kNeg1152, b[0][2 * j], b[0][2 * j + 1], c0[j]);
-    F16Op::mma(c0[j], kNeg1152, kNeg1152, kNeg1152, kNeg1152, b[1][2 * j], b[1][2 * j + 1], c0[j]);
-  }
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int r = 0; r < WARP_SUBTILES; ++r) {
     const uint32_t unit = wunit0 + (uint32_t)(r * Q8_UNIT_BYTES);
     const uint4 codes = lds128(unit + 16u * lane);
     const uint32_t dpair = lds32(unit + 512u + 4u * g);  // (d[g], d[g + 8])
     // word v: k16 step v / 2, half v % 2 -> A registers (a0, a1) or (a2, a3)
-    const uint32_t a00 = u8x2_to_f16x2_biased(codes.x, 0x4140u), a01 = u8x2_to_f16x2_biased(codes.x, 0x4342u);
-    const uint32_t a02 = u8x2_to_f16x2_biased(codes.y, 0x4140u), a03 = u8x2_to_f16x2_biased(codes.y, 0x4342u);
-    const uint32_t a10 = u8x2_to_f16x2_biased(codes.z, 0x4140u), a11 = u8x2_to_f16x2_biased(codes.z, 0x4342u);
-    const uint32_t a12 = u8x2_to_f16x2_biased(codes.w, 0x4140u), a13 = u8x2_to_f16x2_biased(codes.w, 0x4342u);
+    const uint32_t a00 = u8x2_to_f16x2(codes.x, 0x4140u), a01 = u8x2_to_f16x2(codes.x, 0x4342u);
+    const uint32_t a02 = u8x2_to_f16x2(codes.y, 0x4140u), a03 = u8x2_to_f16x2(codes.y, 0x4342u);
+    const uint32_t a10 = u8x2_to_f16x2(codes.z, 0x4140u), a11 = u8x2_to_f16x2(codes.z, 0x4342u);
+    const uint32_t a12 = u8x2_to_f16x2(codes.w, 0x4140u), a13 = u8x2_to_f16x2(codes.w, 0x4342u);
     const float dg = __half2float(__ushort_as_half((unsigned short)(dpair & 0xFFFF)));
     const float dg8 = __half2float(__ushort_as_half((unsigned short)(dpair >> 16)));
 #pragma unroll
     for (int j = 0; j < NT8; ++j) {
       float pp[4];
-      F16Op::mma(pp, a00, a01, a02, a03, b[0][2 * j], b[0][2 * j + 1], c0[j]);
+      F16Op::mma(pp, a00, a01, a02, a03, b[0][2 * j], b[0][2 * j + 1], zero);
       F16Op::mma(pp, a10, a11, a12, a13, b[1][2 * j], b[1][2 * j + 1], pp);
       ffma2(acc[r][j][0], acc[r][j][1], dg, pp[0], pp[1]);
       ffma2(acc[r][j][2], acc[r][j][3], dg8, pp[2], pp[3]);

@@ -45,6 +45,8 @@ SHAPES = {
     # Q8_0 shapes (the FP8 MLP shape and the attention-projection shape)
     "q8_mlp": dict(fmt="q8_0", N=17408, K=5120, Ms=(1, 8, 16), seed=6, outliers=True),
     "q8_attn": dict(fmt="q8_0", N=5120, K=5120, Ms=(1, 8, 16), seed=7, outliers=True),
+    # Q4_0 qkv-projection-like shape of the whole-model sweep (5120 -> 10240)
+    "q4_qkv": dict(fmt="q4_0", N=10240, K=5120, Ms=(1, 8, 16), seed=8, outliers=True),
     # Q4_0 output head (vocabulary 151,936 x hidden 5120) for the greedy acceptance step
     "q4_lmhead": dict(fmt="q4_0", N=151936, K=5120, Ms=(1, 8, 16), seed=5, outliers=True),
 }

@@ -164,3 +164,49 @@ def test_greedy_full_size_output_head():
     a = synth.activations(3, K, b + 1000, outliers=spec["outliers"], outlier_seed=b + 2000)
     check_greedy(mat, O.FMT_Q4_0, blocks, None, N, K, a, False, 1, "greedy output head M=3")
     mat.close()
+
+
+@pytest.mark.parametrize("variant", ["mma", "split3", "simt"])
+@pytest.mark.parametrize("M", [1, 6, 16])
+def test_greedy_nan_scores(variant, M):
+    """Non-finite scores follow the oracle's rule: a NaN ranks above every
+    number and the first NaN of a row wins.  Rows 357 and 801 of W get one
+    block with a NaN fp16 scale, so their scores are NaN for every drafted
+    row, placed after where the finite maximum falls; one drafted row gets a
+    NaN activation, so all of its scores are NaN and its argmax is 0."""
+    N, K = 1000, 512
+    kw = {"k_splits": 3} if variant == "split3" else ({"simt": True} if variant == "simt" else {})
+    w = synth.weights(N, K, 350)
+    w[:40] *= 4.0  # the largest finite scores fall in the first rows
+    blocks = O.q4_0_quantize(w)
+    for n, b in ((357, 5), (801, 11)):
+        blocks[n, b, 0], blocks[n, b, 1] = 0x00, 0x7E  # fp16 NaN
+    mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K, **kw)
+    a = synth.activations(M, K, 351 + M, outliers=True)
+    nan_row = M // 2 if M > 1 else None
+    if nan_row is not None:
+        a[nan_row, 77] = 0x7FC0  # bf16 NaN
+    ref, S = O.verify_rows(O.FMT_Q4_0, blocks, None, N, K, a)
+    ref_am, _, _ = O.greedy_accept(ref.astype(np.float32).astype(np.float64), np.zeros(M, np.int32))
+    finite_best = np.argmax(np.where(np.isnan(ref), -np.inf, ref), axis=1)
+    for m in range(M):
+        assert ref_am[m] == (0 if m == nan_row else 357)
+        if m != nan_row:
+            assert finite_best[m] < 357  # the NaN lies after the finite maximum
+    tokens = block_tokens(ref_am, M - 1, N, 352)
+    out, am, acc = mat.verify_greedy(bf16_cuda(a), torch.from_numpy(tokens).cuda())
+    torch.cuda.synchronize()
+    assert mat.sync_status() == q.QMM_OK
+    got = out.cpu().double().numpy()
+    assert (np.isnan(got) == np.isnan(ref)).all(), "NaN positions differ from the oracle's"
+    fin = ~np.isnan(ref)
+    err = np.abs(got[fin] - ref[fin])
+    assert (err <= 1e-3 * S[fin] + 1e-6).all(), "finite scores out of tolerance"
+    am = am.cpu().numpy()
+    assert (am == ref_am).all(), f"argmax {am.tolist()} != oracle {ref_am.tolist()}"
+    k, nxt = (int(v) for v in acc.cpu().numpy())
+    kk = 0
+    while kk < M - 1 and ref_am[kk] == tokens[kk + 1]:
+        kk += 1
+    assert (k, nxt) == (kk, int(ref_am[kk]))
+    mat.close()

@@ -210,10 +210,13 @@ def test_leading_dimensions_and_untouched_memory():
 FULL = [
     ("q4_attn", (1, 8, 16), False),
     ("q4_attn_tc", (1, 16), False),
+    ("q4_qkv", (1, 8, 16), False),
     ("q4_gateup", (16,), False),
     ("q4_down", (16,), False),
     ("q4_gateup", (16,), True),
     ("q4_down", (16,), True),
+    ("q4_gateup", (16,), 128),
+    ("q4_down", (16,), 128),
     ("fp8_mlp", (1, 8, 16), False),
 ]
 
@@ -232,7 +235,12 @@ def test_full_size_sampled_rows(name, Ms, hadamard):
                                      [0, 1, N - 2, N - 1], rng.choice(N, 200, replace=False)]))
     rows = rows[rows < N].astype(np.int64)
     if spec["fmt"] == "q4_0":
-        blocks = O.q4_0_quantize_h32(w) if hadamard else O.q4_0_quantize(w)
+        if hadamard is True:
+            blocks = O.q4_0_quantize_h32(w)
+        elif hadamard:
+            blocks = O.q4_0_quantize(O.rotate_weights_f32(w, hadamard))
+        else:
+            blocks = O.q4_0_quantize(w)
         del w
         mat = q.Matrix(q.QMM_FMT_Q4_0, torch.from_numpy(blocks).cuda(), N, K, hadamard=hadamard,
                        tcgen05=tc)
