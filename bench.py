@@ -9,6 +9,18 @@ activation pre-pass and the verify kernel per call, chained with
 programmatic dependent launch) and timed with CUDA events on the launching
 stream.  value = compressed weight bytes streamed per step / step time.
 
+The default run then times the other target configurations the same way
+(fewer steps) and reports each under config.per_workload with its own per-M
+figures, roofline fraction, recorded DRAM traffic ratio and M=16/M=1 time
+ratio: FP8 17408x5120 at M = 1/8/16, gate+up and down at M = 16 plain and
+with the 32-point rotation, and the 64-layer whole-model sweep
+(--no-extras skips them).
+
+e2e is the same step through the host-buffer entry point qmm_verify_host:
+every call copies its bf16 rows from pinned host memory, runs the product and
+copies its fp32 result back before it returns.  e2e.graph_value is the step
+as captured CUDA graphs of qmm_verify calls with torch copies around them.
+
 Other workloads (--workload): q4_gateup, q4_down, q4_gateup_h, q4_down_h
 (32-point rotation), q4_gateup_h128, q4_down_h128 (128-point rotation),
 q8_mlp, q8_attn (Q8_0 at the FP8 MLP and the attention shapes),
@@ -244,19 +256,12 @@ def capture(torch, fn):
     return g
 
 
-def run_gpu(args, ws, rank, local):
-    import torch
-    import speculative_decode_verification_qmm_gb300 as q
-    from speculative_decode_verification_qmm_gb300 import synth
-
-    torch.cuda.set_device(local)
-    q.load()
-    dev = torch.device("cuda", local)
-
-    # ---- workload setup (untimed)
+def setup_workload(q, synth, torch, dev, args, workload):
+    """Build the handles, activations and outputs of one workload (untimed).
+    Returns a dict: groups [(M, [(mat, act, out)])], desc, kernel, dtype,
+    greedy buffers."""
     groups = []  # list of (M, [(mat, act, out)])
-    if args.workload == "model":
-        shape_desc = []
+    if workload == "model":
         acts = {}
         mats = []
         for layer in range(synth.MODEL_LAYERS):
@@ -268,8 +273,7 @@ def run_gpu(args, ws, rank, local):
                                      **KERNEL_FLAGS[args.kernel]))
                 del blocks
         torch.cuda.synchronize()
-        Ms = synth.MODEL_MS
-        for M in Ms:
+        for M in synth.MODEL_MS:
             items = []
             # one contiguous output buffer per M (the results read back per step)
             flat = torch.empty(sum(M * m.N for m in mats), dtype=torch.float32, device=dev)
@@ -282,15 +286,13 @@ def run_gpu(args, ws, rank, local):
                 off += M * m.N
                 items.append((m, acts[key], out))
             groups.append((M, items))
-        per_copy_bytes = sum(m.info()["weight_bytes"] for m in mats)
-        copies = 1
-        workload_desc = (f"whole-model Q4_0 sweep: {synth.MODEL_LAYERS} layers x "
-                         f"{{qkv 10240x5120, out 5120x5120, gate+up 34816x5120, down 5120x17408}}, "
-                         f"{per_copy_bytes / 2**30:.2f} GiB compressed per pass, one pass per M")
-        main_kernel = "verify_kernel<0"
-        dtype = "bf16"
+        per_copy = sum(m.info()["weight_bytes"] for m in mats)
+        desc = (f"whole-model Q4_0 sweep: {synth.MODEL_LAYERS} layers x "
+                f"{{qkv 10240x5120, out 5120x5120, gate+up 34816x5120, down 5120x17408}}, "
+                f"{per_copy / 2**30:.2f} GiB compressed per pass, one pass per M")
+        kernel, dtype, l2 = "verify_kernel<0", "bf16", "inputs larger than L2 (11.6 GiB per pass)"
     else:
-        shape_name, hadamard, Ms = WORKLOADS[args.workload]
+        shape_name, hadamard, Ms = WORKLOADS[workload]
         spec = synth.SHAPES[shape_name]
         N, K = spec["N"], spec["K"]
         one = {"q4_0": N * K // 32 * 18, "q8_0": N * K // 32 * 34}.get(
@@ -303,24 +305,29 @@ def run_gpu(args, ws, rank, local):
             outbuf = torch.empty((len(mats), M, N), dtype=torch.float32, device=dev)
             items = [(m, act, outbuf[i]) for i, m in enumerate(mats)]
             groups.append((M, items))
-        per_copy_bytes = one
         fmt_name = {"q4_0": "Q4_0", "q8_0": "Q8_0"}.get(spec["fmt"], "FP8 E4M3 128x128")
         rot = f" Hadamard{32 if hadamard is True else hadamard}" if hadamard else ""
-        workload_desc = (f"{fmt_name} verify K={K} N={N}{rot}, "
-                         f"M={'/'.join(map(str, Ms))}, {copies} distinct weight copies "
-                         f"({copies * one / 1e6:.0f} MB, > 4x L2) cycled")
-        main_kernel = "verify_kernel<" + {"q4_0": "0", "q8_0": "2"}.get(spec["fmt"], "1")
+        desc = (f"{fmt_name} verify K={K} N={N}{rot}, "
+                f"M={'/'.join(map(str, Ms))}, {copies} distinct weight copies "
+                f"({copies * one / 1e6:.0f} MB, > 4x L2) cycled")
+        kernel = "verify_kernel<" + {"q4_0": "0", "q8_0": "2"}.get(spec["fmt"], "1")
         dtype = "f16" if (hadamard or spec["fmt"] != "q4_0") else "bf16"
-
+        l2 = "inputs larger than L2 (distinct weight copies)"
     # the greedy workload: per call the block's tokens (shared per M) and its
     # argmax [M] and accept [2] outputs, in one int32 buffer per M
-    greedy = args.workload == "q4_lmhead"
+    greedy = workload == "q4_lmhead"
     gbufs = {}
     if greedy:
         for M, items in groups:
             tok = torch.zeros(M, dtype=torch.int32, device=dev)
             res = torch.zeros((len(items), M + 2), dtype=torch.int32, device=dev)
             gbufs[M] = (tok, res)
+    return {"name": workload, "groups": groups, "desc": desc, "kernel": kernel, "dtype": dtype,
+            "l2": l2, "greedy": greedy, "gbufs": gbufs}
+
+
+def make_call(q, W):
+    greedy, gbufs = W["greedy"], W["gbufs"]
 
     def call(m, act, out, j=0):
         M = act.shape[0]
@@ -329,24 +336,33 @@ def run_gpu(args, ws, rank, local):
             q.qmm_verify_greedy(m.handle, act, out, M, tok, res[j, :M], res[j, M:])
         else:
             q.qmm_verify(m.handle, act, out, M)
+    return call
+
+
+def time_workload(q, torch, W, steps, warmup, ws, local, dev, peak):
+    """Capture one CUDA graph per M (every call of the group back to back) and
+    time `steps` replays of all of them after `warmup`, with CUDA events on the
+    launching stream; clocks sampled meanwhile.  Returns the per-M breakdown
+    and the step totals."""
+    groups = W["groups"]
+    call = make_call(q, W)
 
     def run_group(items):
         for j, (m, act, out) in enumerate(items):
             call(m, act, out, j)
 
     graphs = [(M, capture(torch, lambda it=items: run_group(it)), items) for M, items in groups]
-    # kernels per call: the verify kernel, plus the activation pre-pass on the f16 paths
     calls_per_step = sum(len(items) for _, items in groups)
     rot_flags = q.QMM_FLAG_HADAMARD32 | q.QMM_FLAG_HADAMARD64 | q.QMM_FLAG_HADAMARD128
+    # kernels per call: the verify kernel, plus the activation pre-pass on the f16 paths
     launches_per_step = sum(sum(1 + int(bool(m.info()["flags"] & rot_flags)
                                         or m.fmt != q.QMM_FMT_Q4_0)
                                 for m, _, _ in items) for _, items in groups)
     bytes_per_step = sum(sum(m.info()["weight_bytes"] for m, _, _ in items) for _, items in groups)
 
-    # ---- warmup (the clock sampler starts here so that it is running by the timed region)
     clocks = ClockSampler(local).__enter__()
     time.sleep(0.5)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         for _, g, _ in graphs:
             g.replay()
     torch.cuda.synchronize()
@@ -356,74 +372,128 @@ def run_gpu(args, ws, rank, local):
             if rc != q.QMM_OK:
                 raise RuntimeError(f"device status after warmup: {q.qmm_strerror(rc)}")
 
-    # ---- timed region: K steps; per-M events on the launching stream
     stream = torch.cuda.current_stream()
-    per_m = {M: 0.0 for M, _, _ in graphs}
     barrier(ws)
     torch.cuda.synchronize()
     n_before = len(clocks.lines)
-    if True:
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        marks = []
-        ev0.record(stream)
-        for _ in range(args.steps):
-            for M, g, _ in graphs:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-                marks.append((M, a, b))
-        ev1.record(stream)
-        torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    marks = []
+    ev0.record(stream)
+    for _ in range(steps):
+        for M, g, _ in graphs:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            marks.append((M, a, b))
+    ev1.record(stream)
+    torch.cuda.synchronize()
     time.sleep(0.25)
     clocks.__exit__(None, None, None)
     clocks.lines = clocks.lines[max(0, n_before - 2):]
     barrier(ws)
     total_ms = ev0.elapsed_time(ev1)
+    per_m = {M: 0.0 for M, _, _ in graphs}
     per_m_samples = {M: [] for M, _, _ in graphs}
     for M, a, b in marks:
         dt = a.elapsed_time(b)
         per_m[M] += dt
         per_m_samples[M].append(dt)
     total_ms = max_over_ranks(total_ms, ws, dev)
-    ms_per_step = total_ms / args.steps
-    total_bytes = sum_over_ranks(bytes_per_step * args.steps, ws, dev)
-    value = total_bytes / (total_ms * 1e-3) / 1e9
-    clk = clocks.summary()
-
     for _, items in groups:
         for m, _, _ in items:
             rc = m.sync_status()
             if rc != q.QMM_OK:
                 raise RuntimeError(f"device status after timing: {q.qmm_strerror(rc)}")
 
-    peak, peak_kind = measured_peak_gbs()
-    per_launch_bytes = bytes_per_step / calls_per_step
-    avg_launch_s = (ms_per_step * 1e-3) / calls_per_step
-    achieved = per_launch_bytes / avg_launch_s / 1e9
-    m_breakdown = {}
+    breakdown = {}
     for M, _, items in graphs:
         b = sum(m.info()["weight_bytes"] for m, _, _ in items)
-        t = per_m[M] / args.steps
+        t = per_m[M] / steps
         xs = sorted(per_m_samples[M])
         qt = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
         med = statistics.median(xs)
         # one verify pass = one call on one matrix (the model workload: the
         # whole 64-layer sweep)
-        passes = 1 if args.workload == "model" else len(items)
-        m_breakdown[str(M)] = {"ms": round(t, 5), "GBps": round(b / (t * 1e-3) / 1e9, 1),
-                               "pct_of_peak": round(100 * b / (t * 1e-3) / 1e9 / peak, 1),
-                               "ms_median": round(med, 5), "ms_p10": round(qt(0.1), 5),
-                               "ms_p90": round(qt(0.9), 5),
-                               "GBps_median": round(b / (med * 1e-3) / 1e9, 1),
-                               "verify_passes_per_s": round(passes / (med * 1e-3), 1)}
+        passes = 1 if W["name"] == "model" else len(items)
+        breakdown[str(M)] = {"ms": round(t, 5), "GBps": round(b / (t * 1e-3) / 1e9, 1),
+                             "pct_of_peak": round(100 * b / (t * 1e-3) / 1e9 / peak, 1),
+                             "ms_median": round(med, 5), "ms_p10": round(qt(0.1), 5),
+                             "ms_p90": round(qt(0.9), 5),
+                             "GBps_median": round(b / (med * 1e-3) / 1e9, 1),
+                             "verify_passes_per_s": round(passes / (med * 1e-3), 1),
+                             "us_per_call": round(t * 1e3 / len(items), 3)}
+    return {"graphs": graphs, "per_M": breakdown, "total_ms": total_ms,
+            "ms_per_step": total_ms / steps, "calls_per_step": calls_per_step,
+            "launches_per_step": launches_per_step, "bytes_per_step": bytes_per_step,
+            "clocks": clocks.summary()}
+
+
+def m16_over_m1(breakdown):
+    if "16" in breakdown and "1" in breakdown:
+        return round(breakdown["16"]["ms"] / breakdown["1"]["ms"], 3)
+    return None
+
+
+# The other target configurations, timed after the headline one in the default
+# run and reported under config.per_workload: FP8 at M = 1/8/16, gate+up and
+# down at M = 16 plain and with the 32-point rotation, and the 64-layer sweep.
+EXTRA_WORKLOADS = ("fp8_mlp", "q4_gateup", "q4_down", "q4_gateup_h", "q4_down_h", "model")
+
+
+def extra_entry(q, torch, synth, dev, args, name, ws, local, peak):
+    W = setup_workload(q, synth, torch, dev, args, name)
+    steps = max(1, min(args.steps, 10))
+    T = time_workload(q, torch, W, steps, 3, ws, local, dev, peak)
+    achieved = (T["bytes_per_step"] / T["calls_per_step"]) / (T["ms_per_step"] * 1e-3 /
+                                                               T["calls_per_step"]) / 1e9
+    first = W["groups"][0][1][0][0]
+    traffic = recorded_traffic(name)
+    per_launch = T["bytes_per_step"] / T["calls_per_step"]
+    entry = {"workload": W["desc"], "dtype": W["dtype"], "l2": W["l2"], "steps": steps,
+             "kernel": W["kernel"],
+             "plan": {k: first.info()[k] for k in
+                      ("n_tiles", "k_splits", "ctas", "stages_per_cta", "pipeline_depth")},
+             "per_M": T["per_M"], "GBps": round(achieved, 1),
+             "roofline_frac": round(achieved / peak, 3),
+             "traffic_ratio": (round(traffic / per_launch, 4) if traffic and name != "model"
+                               else None),
+             "m16_over_m1_time": m16_over_m1(T["per_M"]), "clocks": T["clocks"]}
+    del T, W
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_gpu(args, ws, rank, local):
+    import torch
+    import speculative_decode_verification_qmm_gb300 as q
+    from speculative_decode_verification_qmm_gb300 import synth
+
+    torch.cuda.set_device(local)
+    q.load()
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peak_gbs()
+
+    W = setup_workload(q, synth, torch, dev, args, args.workload)
+    groups = W["groups"]
+    call = make_call(q, W)
+    T = time_workload(q, torch, W, args.steps, args.warmup, ws, local, dev, peak)
+    m_breakdown = T["per_M"]
+    ms_per_step = T["ms_per_step"]
+    total_bytes = sum_over_ranks(T["bytes_per_step"] * args.steps, ws, dev)
+    value = total_bytes / (T["total_ms"] * 1e-3) / 1e9
+    per_launch_bytes = T["bytes_per_step"] / T["calls_per_step"]
+    avg_launch_s = (ms_per_step * 1e-3) / T["calls_per_step"]
+    achieved = per_launch_bytes / avg_launch_s / 1e9
+    stream = torch.cuda.current_stream()
 
     # ---- one isolated call per M after an L2 flush (a 2 x L2 buffer written
     # first; the events bracket the call only): no neighbour to overlap with
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-    for M, _, items in graphs:
+    for M, _, items in T["graphs"]:
         m0, act0, out0 = items[0]
         iso = []
         for _ in range(5):
@@ -438,71 +508,96 @@ def run_gpu(args, ws, rank, local):
         m_breakdown[str(M)]["isolated_call_us"] = round(statistics.median(iso), 2)
     del flush
 
-    # ---- end to end through the public API: every step copies its
-    # activations from pinned host memory to the device, makes its verify
-    # calls (qmm_verify, one per matrix and M), copies all of its results back
-    # into pinned host memory, and waits for them.  The calls run as the CUDA
-    # graphs captured above through the same API (an engine keeps its decode
-    # step in one graph); the same step with every call launched eagerly from
-    # Python is reported beside it.
+    # ---- end to end through the public host-buffer call: per step, every call
+    # of the step goes through qmm_verify_host with pinned host buffers at both
+    # ends (the call copies its activation rows to the device, runs the verify
+    # product and copies its fp32 result back before returning).  The same step
+    # run as the captured CUDA graphs with torch copies around them is reported
+    # beside it (graph_value).
     e2e = None
     if not args.no_e2e:
-        plan = []  # per M: (device inputs, pinned host inputs, items, device outputs, pinned host outputs)
+        host_in = {}
+        plan = []  # per call: (mat, pinned act, pinned out)
+        for M, items in groups:
+            for m, act, out in items:
+                key = act.data_ptr()
+                if key not in host_in:
+                    host_in[key] = act.cpu().pin_memory()
+                plan.append((m, host_in[key], torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()))
+        h2d = sum(hi.numel() * 2 for _, hi, _ in plan)
+        d2h = sum(ho.numel() * 4 for _, _, ho in plan)
+        greedy = W["greedy"]
+
+        def host_step():
+            for m, hi, ho in plan:
+                q.qmm_verify_host(m.handle, hi, ho, hi.shape[0])
+
+        e2e_steps = max(1, min(args.steps, 5))
+
+        def wall(fn):
+            fn()  # warm
+            barrier(ws)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                fn()
+            return max_over_ranks(time.perf_counter() - t0, ws, dev)
+
+        e2e_bytes = sum_over_ranks(T["bytes_per_step"] * e2e_steps, ws, dev)
+        e2e = {"unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps}
+        if not greedy:
+            el = wall(host_step)
+            e2e["value"] = round(e2e_bytes / el / 1e9, 1)
+            e2e["api"] = ("qmm_verify_host (host buffers): every call of the step copies its "
+                          "bf16 rows from pinned host memory, runs the verify product and copies "
+                          "its fp32 result back to pinned host memory before returning")
+        # the graph form: per M, the activations copied in, the captured graph
+        # replayed, every output copied back; one synchronize per step
+        gplan = []
         for M, items in groups:
             ins = []
             for _, act, _ in items:
                 if all(act.data_ptr() != d.data_ptr() for d, _ in ins):
                     ins.append((act, act.cpu().pin_memory()))
             if greedy:  # the step's result is the decision: argmax and accepted count per call
-                dev_out = gbufs[M][1].view(-1)
-                plan.append((ins, items, dev_out, torch.empty(dev_out.numel(), dtype=torch.int32).pin_memory()))
+                dev_out = W["gbufs"][M][1].view(-1)
+                gplan.append((ins, dev_out, torch.empty(dev_out.numel(), dtype=torch.int32).pin_memory()))
                 continue
             base = items[0][2]
             n_out = sum(out.numel() for _, _, out in items)
             dev_out = torch.as_strided(base, (n_out,), (1,))  # the contiguous buffer behind the views
-            plan.append((ins, items, dev_out, torch.empty(n_out, dtype=torch.float32).pin_memory()))
-        h2d = sum(hi.numel() * 2 for ins, _, _, _ in plan for _, hi in ins)
-        d2h = sum(ho.numel() * ho.element_size() for _, _, _, ho in plan)
+            gplan.append((ins, dev_out, torch.empty(n_out, dtype=torch.float32).pin_memory()))
+        graph_of = {M: g for M, g, _ in T["graphs"]}
 
-        graph_of = {M: g for M, g, _ in graphs}
-
-        def e2e_step(graph_mode):
-            for (M, _), (ins, items, dev_out, host_out) in zip(groups, plan):
+        def graph_step():
+            for (M, _), (ins, dev_out, host_out) in zip(groups, gplan):
                 for d, hi in ins:
                     d.copy_(hi, non_blocking=True)
-                if graph_mode:
-                    graph_of[M].replay()
-                else:
-                    for j, (m, act, out) in enumerate(items):
-                        call(m, act, out, j)
+                graph_of[M].replay()
                 host_out.copy_(dev_out, non_blocking=True)
             torch.cuda.synchronize()
 
-        e2e_steps = max(1, min(args.steps, 5))
-
-        def e2e_time(graph_mode):
-            e2e_step(graph_mode)  # warm
-            barrier(ws)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for _ in range(e2e_steps):
-                e2e_step(graph_mode)
-            return max_over_ranks(time.perf_counter() - t0, ws, dev)
-
-        el = e2e_time(True)
-        el_eager = e2e_time(False)
-        e2e_bytes = sum_over_ranks(bytes_per_step * e2e_steps, ws, dev)
-        e2e = {"value": round(e2e_bytes / el / 1e9, 1), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": e2e_steps,
-               "api": "qmm_verify (device buffers): per step the activations are copied from "
-                      "pinned host memory, the step's calls run as a CUDA graph captured through "
-                      "qmm_verify, all outputs are copied back to pinned host memory, then one "
-                      "synchronize",
-               "eager_value": round(e2e_bytes / el_eager / 1e9, 1),
-               "eager_api": "the same step with every qmm_verify call launched eagerly from Python"}
+        elg = wall(graph_step)
+        e2e["graph_value"] = round(e2e_bytes / elg / 1e9, 1)
+        e2e["graph_api"] = ("qmm_verify captured in CUDA graphs: per step the activations are "
+                            "copied from pinned host memory, the graphs replayed, all outputs "
+                            "copied back to pinned host memory, one synchronize")
+        if greedy:
+            e2e["value"] = e2e["graph_value"]
+            e2e["h2d_bytes_per_step"] = sum(hi.numel() * 2 for ins, _, _ in gplan for _, hi in ins)
+            e2e["d2h_bytes_per_step"] = sum(ho.numel() * 4 for _, _, ho in gplan)
+            e2e["api"] = e2e["graph_api"] + " (the step's result is the decision: argmax and k)"
 
     traffic = recorded_traffic(args.workload)
+    first = groups[0][1][0][0]
+    per_workload = {}
+    gpu_launches = T["launches_per_step"] * args.steps
+    main_clocks = T["clocks"]
+    del T
+    if args.workload == "q4_attn" and not args.no_extras:
+        for name in EXTRA_WORKLOADS:
+            per_workload[name] = extra_entry(q, torch, synth, dev, args, name, ws, local, peak)
     line = {
         "metric": "verify-matmul weight GB/s (% of GB300 HBM peak) at M=1/8/16 draft rows",
         "value": round(value, 1),
@@ -514,25 +609,25 @@ def run_gpu(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": dtype,
+        "dtype": W["dtype"],
         "data": "synthetic (seeded N(0,0.02) weights quantized on the device, bf16 N(0,1) "
                 "activations with 0.1% x20 outlier channels)",
-        "config": {"workload": workload_desc, "l2": "inputs larger than L2 (distinct weight copies)",
-                   "plan": {k: groups[0][1][0][0].info()[k] for k in
+        "config": {"workload": W["desc"], "l2": W["l2"],
+                   "plan": {k: first.info()[k] for k in
                             ("n_tiles", "k_splits", "ctas", "stages_per_cta", "pipeline_depth")},
                    "parallelism": f"replicas x{ws}", "per_M": m_breakdown,
                    "pct_of_peak": round(100 * value / ws / peak, 1),
-                   "m16_over_m1_time": (round(m_breakdown["16"]["ms"] / m_breakdown["1"]["ms"], 3)
-                                        if "16" in m_breakdown and "1" in m_breakdown else None)},
-        "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": round(achieved, 1),
+                   "m16_over_m1_time": m16_over_m1(m_breakdown),
+                   "per_workload": per_workload or None},
+        "roofline": {"bound": "hbm", "kernel": W["kernel"], "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} (STREAM-style copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 3),
                      "traffic": traffic, "algorithmic_bytes_per_launch": int(per_launch_bytes),
                      "note": "verify-kernel launch duration averaged over the timed region "
                              "(back-to-back calls; any activation pre-pass included)"},
-        "clocks": clk,
+        "clocks": main_clocks,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": gpu_launches,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
@@ -842,6 +937,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload only: skip the other target configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
