@@ -33,7 +33,9 @@ metric, TFLOP/s against the dense f16/bf16 tensor peak).
 Multi-GPU (--gpus N under torchrun): the path shards into independent
 problems, so every rank runs its own replica of the workload with no
 collective on the data path; ranks meet only at the timing barrier and the
-max-over-ranks reduction of the elapsed time ("scaling": "weak").
+max-over-ranks reduction of the elapsed time ("scaling": "weak").  --shard
+instead splits each matrix by rows over the ranks (qmm_create_rows) and
+all-gathers every call's [M, N/G] output with NCCL ("scaling": "strong").
 
 --impl reference times the CPU oracle (the plain fp64 triple loop) on a
 bounded sample of the same workload on the host cores.
@@ -105,6 +107,26 @@ def sum_over_ranks(x: float, ws: int, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def gather_shards(part, N: int, ws: int, align: int = 1):
+    """All-gather the [M, N_g] outputs of the ranks' row shards into [M, N]:
+    rank g computed columns shard_rows(N, ws, g, align) of the product.  The
+    shards are padded to the widest one for the collective.  One rank: the
+    part itself."""
+    if ws <= 1:
+        return part
+    import torch
+    import torch.distributed as dist
+    from speculative_decode_verification_qmm_gb300 import shard_rows
+    M = part.shape[0]
+    sizes = [shard_rows(N, ws, g, align) for g in range(ws)]
+    width = max(b - a for a, b in sizes)
+    buf = torch.zeros((M, width), dtype=part.dtype, device=part.device)
+    buf[:, :part.shape[1]] = part
+    outs = [torch.empty_like(buf) for _ in range(ws)]
+    dist.all_gather(outs, buf)
+    return torch.cat([o[:, :b - a] for o, (a, b) in zip(outs, sizes)], dim=1)
 
 
 def barrier(ws: int):
@@ -214,7 +236,9 @@ KERNEL_FLAGS = {"auto": {}, "mma": {}, "tc": {"tcgen05": True}, "simt": {"simt":
 
 
 def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, splits=0,
-                   kernel="auto"):
+                   kernel="auto", rows=None):
+    """`copies` handles of the named shape (distinct seeded weights); rows =
+    (n_begin, n_end): handles over those rows only (a shard of the split)."""
     spec = synth.SHAPES[shape_name]
     kf = KERNEL_FLAGS[kernel]
     N, K = spec["N"], spec["K"]
@@ -225,18 +249,19 @@ def build_matrices(q, synth, shape_name, hadamard, copies, torch, seed_base=0, s
             blocks = q.quantize_q4_0(w, hadamard=hadamard)
             del w
             mats.append(q.Matrix(q.QMM_FMT_Q4_0, blocks, N, K, hadamard=hadamard, k_splits=splits,
-                                 **kf))
+                                 rows=rows, **kf))
             del blocks
         elif spec["fmt"] == "q8_0":
             blocks = q.quantize_q8_0(w, hadamard=hadamard)
             del w
-            mats.append(q.Matrix(q.QMM_FMT_Q8_0, blocks, N, K, hadamard=hadamard, k_splits=splits))
+            mats.append(q.Matrix(q.QMM_FMT_Q8_0, blocks, N, K, hadamard=hadamard, k_splits=splits,
+                                 rows=rows))
             del blocks
         else:
             codes, scales = q.quantize_fp8(w, hadamard=hadamard)
             del w
             mats.append(q.Matrix(q.QMM_FMT_FP8_E4M3_B128, codes, N, K, scales=scales,
-                                 hadamard=hadamard, k_splits=splits))
+                                 hadamard=hadamard, k_splits=splits, rows=rows))
             del codes, scales
     torch.cuda.synchronize()
     return mats, spec
@@ -634,6 +659,106 @@ def run_gpu(args, ws, rank, local):
     return line, rank
 
 
+# ---------------------------------------------------------------- row split
+def run_shard(args, ws, rank, local):
+    """--shard: the matrix is split by rows over the ranks (rank g holds rows
+    [g N / G, (g + 1) N / G), multiples of 128 for FP8) and every verify call
+    is followed by the all-gather of the [M, N / G] fp32 parts into the full
+    [M, N] output (NCCL), the one exchange the split needs.  One step: at each
+    M, every weight copy's call and gather.  value = compressed bytes of the
+    whole matrices per step / step time (max over ranks); "scaling": "strong"
+    (the total work is fixed as the ranks grow)."""
+    import torch
+    import speculative_decode_verification_qmm_gb300 as q
+    from speculative_decode_verification_qmm_gb300 import synth
+
+    if args.workload not in WORKLOADS or args.workload == "q4_lmhead":
+        raise SystemExit("--shard takes one of the single-matrix verify workloads")
+    torch.cuda.set_device(local)
+    q.load()
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peak_gbs()
+    shape_name, hadamard, Ms = WORKLOADS[args.workload]
+    spec = synth.SHAPES[shape_name]
+    N, K = spec["N"], spec["K"]
+    align = 128 if spec["fmt"] == "fp8" else 1
+    rows = q.shard_rows(N, ws, rank, align)
+    one = {"q4_0": N * K // 32 * 18, "q8_0": N * K // 32 * 34}.get(
+        spec["fmt"], N * K + 4 * (N // 128) * (K // 128))
+    part_bytes = one * (rows[1] - rows[0]) / N
+    copies = args.copies or max(2, int(-(-4 * L2_BYTES // part_bytes)))
+    mats, _ = build_matrices(q, synth, shape_name, hadamard, copies, torch, splits=args.splits,
+                             kernel=args.kernel, rows=rows)
+    acts = {M: synth.activations_cuda(M, K, spec["seed"] + 1000, outliers=spec["outliers"])
+            for M in Ms}
+    outs = {M: [torch.empty((M, rows[1] - rows[0]), dtype=torch.float32, device=dev) for _ in mats]
+            for M in Ms}
+
+    def step_m(M):
+        for m, o in zip(mats, outs[M]):
+            q.qmm_verify(m.handle, acts[M], o, M)
+            gather_shards(o, N, ws, align)
+
+    clocks = ClockSampler(local).__enter__()
+    time.sleep(0.5)
+    for _ in range(args.warmup):
+        for M in Ms:
+            step_m(M)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    n_before = len(clocks.lines)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per_m = {M: 0.0 for M in Ms}
+    ev0.record(stream)
+    for _ in range(args.steps):
+        for M in Ms:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_m(M)
+            b.record(stream)
+            torch.cuda.synchronize()
+            per_m[M] += a.elapsed_time(b)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.__exit__(None, None, None)
+    clocks.lines = clocks.lines[max(0, n_before - 2):]
+    barrier(ws)
+    for m in mats:
+        if m.sync_status() != q.QMM_OK:
+            raise RuntimeError("device status after timing")
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
+    full_bytes = one * copies * len(Ms) * args.steps
+    value = full_bytes / (total_ms * 1e-3) / 1e9
+    per_M = {}
+    for M in Ms:
+        t = max_over_ranks(per_m[M], ws, dev) / args.steps
+        per_M[str(M)] = {"ms": round(t, 5), "GBps": round(one * copies / (t * 1e-3) / 1e9, 1),
+                         "us_per_call_and_gather": round(t * 1e3 / copies, 3)}
+    line = {
+        "metric": "verify-matmul weight GB/s (% of GB300 HBM peak) at M=1/8/16 draft rows",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "f16" if (hadamard or spec["fmt"] != "q4_0") else "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights quantized on the device, bf16 N(0,1) "
+                "activations with 0.1% x20 outlier channels)",
+        "config": {"workload": f"{args.workload} split by rows over {ws} GPU(s), rows "
+                               f"{rows[0]}..{rows[1]} on rank {rank}, {copies} weight copies, "
+                               "NCCL all-gather of every call's [M, N/G] output",
+                   "l2": "inputs larger than L2 (distinct weight copies)",
+                   "parallelism": f"row split x{ws}", "per_M": per_M,
+                   "pct_of_peak": round(100 * value / ws / peak, 1)},
+        "roofline": None,
+        "clocks": clocks.summary(),
+        "e2e": None,
+        "gpu_launches": copies * len(Ms) * args.steps * (1 + int(bool(hadamard) or spec["fmt"] != "q4_0")),
+    }
+    return line, rank
+
+
 # ---------------------------------------------------------------- prefill GEMM
 PREFILL_METRIC = "prefill FP8 GEMM TFLOP/s (% of GB300 dense bf16/f16 peak) at M=512/2048/8192 prompt rows"
 PREFILL_MS = (512, 2048, 8192)
@@ -939,6 +1064,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="default workload only: skip the other target configurations")
+    ap.add_argument("--shard", action="store_true",
+                    help="split each matrix by rows over the ranks and all-gather every "
+                         "call's output (strong scaling) instead of running replicas")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -957,6 +1085,8 @@ def main(argv=None):
         dist.init_process_group("nccl")
     if args.workload == "fp8_prefill":
         line, rank = run_prefill(args, ws, rank, local)
+    elif args.shard:
+        line, rank = run_shard(args, ws, rank, local)
     else:
         line, rank = run_gpu(args, ws, rank, local)
     if rank == 0:

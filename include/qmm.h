@@ -161,6 +161,22 @@ typedef struct {
  * failure; nothing is leaked and *out is set to NULL). */
 int qmm_create(qmm_t* out, const qmm_desc* desc, void* stream);
 
+/* A handle over the rows [n_begin, n_end) of the matrix `desc` describes
+ * (desc->N, desc->weights and desc->scales describe the whole W[N][K]): its
+ * matrix is W[n_begin .. n_end - 1], N' = n_end - n_begin rows, so qmm_verify
+ * on it writes out[m][0 .. N' - 1] = columns n_begin .. n_end - 1 of the full
+ * product.  This is the unit of the multi-GPU split: the rows of W are
+ * independent, so GPU g of G takes rows [g N / G, (g + 1) N / G) and computes
+ * its columns with no reduction; an all-gather of the [M][N'] parts assembles
+ * the result (r9k splits its model over two GPUs, "r9k: a from-scratch
+ * inference engine for Qwen3.8-27B on two Radeon AI PRO R9700", opening
+ * section; here the split needs no all-reduce).  Same ownership and
+ * synchronisation as qmm_create.
+ * Errors: as qmm_create, plus SHAPE when n_begin < 0, n_end > N, the range is
+ * empty, or (FP8) n_begin or n_end is not a multiple of 128 (n_end == N
+ * excepted, which is one already). */
+int qmm_create_rows(qmm_t* out, const qmm_desc* desc, int64_t n_begin, int64_t n_end, void* stream);
+
 /* Destroy a handle and free everything it owns (synchronises its device work
  * first).  NULL is accepted.  Using a handle after this returns QMM_ERR_STATE. */
 int qmm_destroy(qmm_t h);

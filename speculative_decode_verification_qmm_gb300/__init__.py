@@ -20,7 +20,7 @@ from ._lib import (QMM_ERR_ALIGN, QMM_ERR_CUDA, QMM_ERR_DEVICE, QMM_ERR_INVALID_
                    QMM_OK, QmmError, load, qmm_desc, qmm_info)
 
 __all__ = [
-    "Matrix", "qmm_create", "qmm_destroy", "qmm_verify", "qmm_verify_greedy", "qmm_verify_host",
+    "Matrix", "qmm_create", "qmm_create_rows", "shard_rows", "qmm_destroy", "qmm_verify", "qmm_verify_greedy", "qmm_verify_host",
     "qmm_verify_noalloc", "qmm_prefill", "qmm_prefill_workspace", "qmm_sync_status",
     "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
     "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
@@ -58,9 +58,11 @@ def qmm_last_cuda_error(h=None) -> int:
 
 
 def qmm_create(fmt: int, weights, N: int, K: int, scales=None, flags: int = 0,
-               k_splits: int = 0, stream=None) -> int:
+               k_splits: int = 0, stream=None, rows=None) -> int:
     """Create a handle.  ``weights``/``scales`` are CUDA tensors (device) or CPU
-    tensors / numpy arrays (host); returns the opaque handle as an int."""
+    tensors / numpy arrays (host); returns the opaque handle as an int.
+    ``rows = (n_begin, n_end)``: a handle over those rows of W only
+    (qmm_create_rows)."""
     import numpy as np
     d = qmm_desc()
     d.struct_size = ctypes.sizeof(qmm_desc)
@@ -89,8 +91,28 @@ def qmm_create(fmt: int, weights, N: int, K: int, scales=None, flags: int = 0,
         raise ValueError("weights and scales must both be on the device or both on the host")
     d.weights_on_device = on_dev
     h = ctypes.c_void_p()
-    _check("qmm_create", load().qmm_create(ctypes.byref(h), ctypes.byref(d), _stream_ptr(stream)))
+    if rows is None:
+        _check("qmm_create", load().qmm_create(ctypes.byref(h), ctypes.byref(d), _stream_ptr(stream)))
+    else:
+        _check("qmm_create_rows", load().qmm_create_rows(ctypes.byref(h), ctypes.byref(d), int(rows[0]),
+                                                         int(rows[1]), _stream_ptr(stream)))
     return h.value
+
+
+def qmm_create_rows(fmt: int, weights, N: int, K: int, n_begin: int, n_end: int, scales=None,
+                    flags: int = 0, k_splits: int = 0, stream=None) -> int:
+    """A handle over rows [n_begin, n_end) of the N-row matrix described."""
+    return qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream, rows=(n_begin, n_end))
+
+
+def shard_rows(N: int, G: int, g: int, align: int = 1):
+    """Rows [n_begin, n_end) of shard g of G for an N-row matrix: the split
+    points g N / G rounded down to a multiple of `align` (128 for FP8), the
+    last shard ending at N."""
+    if not (0 <= g < G):
+        raise ValueError("shard index out of range")
+    cut = lambda x: N if x == G else (N * x // G) // align * align
+    return cut(g), cut(g + 1)
 
 
 def qmm_destroy(h) -> None:
@@ -256,11 +278,16 @@ class Matrix:
     """One weight matrix on the device, ready for repeated verify calls."""
 
     def __init__(self, fmt: int, weights, N: int, K: int, scales=None, hadamard=False,
-                 simt: bool = False, k_splits: int = 0, stream=None, tcgen05: bool = False):
+                 simt: bool = False, k_splits: int = 0, stream=None, tcgen05: bool = False,
+                 rows=None):
+        """``rows = (n_begin, n_end)``: the handle holds only those rows of the
+        N-row matrix the arguments describe (a shard of the multi-GPU split);
+        its product has n_end - n_begin columns."""
         flags = (rotation_flag(hadamard) | (QMM_FLAG_SIMT if simt else 0)
                  | (QMM_FLAG_TCGEN05 if tcgen05 else 0))
-        self.N, self.K, self.fmt = N, K, fmt
-        self.handle = qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream)
+        self.N = N if rows is None else rows[1] - rows[0]
+        self.K, self.fmt, self.rows = K, fmt, rows
+        self.handle = qmm_create(fmt, weights, N, K, scales, flags, k_splits, stream, rows=rows)
 
     def verify(self, act, out=None, stream=None):
         import torch

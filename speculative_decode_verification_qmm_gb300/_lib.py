@@ -73,6 +73,7 @@ _U32 = ctypes.c_uint32
 # name -> (restype, argtypes); every function declared in include/qmm.h
 SIGNATURES = {
     "qmm_create": (_INT, [ctypes.POINTER(_P), ctypes.POINTER(qmm_desc), _P]),
+    "qmm_create_rows": (_INT, [ctypes.POINTER(_P), ctypes.POINTER(qmm_desc), _I64, _I64, _P]),
     "qmm_destroy": (_INT, [_P]),
     "qmm_verify": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P]),
     "qmm_verify_greedy": (_INT, [_P, _P, _I64, _P, _I64, _INT, _P, _P, _P, _P]),

@@ -503,6 +503,33 @@ fail:
   return cuda_fail(nullptr, e);
 }
 
+int qmm_create_rows(qmm_t* out, const qmm_desc* d, int64_t n_begin, int64_t n_end, void* stream) {
+  if (!out) return QMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!d || d->struct_size != sizeof(qmm_desc) || !d->weights) return QMM_ERR_INVALID_ARG;
+  if (d->format != QMM_FMT_Q4_0 && d->format != QMM_FMT_FP8_E4M3_B128 && d->format != QMM_FMT_Q8_0)
+    return QMM_ERR_INVALID_ARG;
+  if (n_begin < 0 || n_end > d->N || n_begin >= n_end) return QMM_ERR_SHAPE;
+  const int fmt = (int)d->format;
+  if (fmt == QMM_FMT_FP8_E4M3_B128 && ((n_begin % 128) || (n_end % 128))) return QMM_ERR_SHAPE;
+  if ((fmt == QMM_FMT_Q4_0 || fmt == QMM_FMT_Q8_0) && d->K % 32) return QMM_ERR_SHAPE;
+  if (fmt == QMM_FMT_FP8_E4M3_B128 && (d->K % 128 || d->N % 128)) return QMM_ERR_SHAPE;
+  // The rows of every format are stored one after another, so the shard is a
+  // sub-range of the caller's buffers (host or device alike).
+  qmm_desc sub = *d;
+  sub.N = n_end - n_begin;
+  const uint8_t* w = reinterpret_cast<const uint8_t*>(d->weights);
+  if (fmt == QMM_FMT_Q4_0) {
+    sub.weights = w + (size_t)n_begin * (size_t)(d->K / 32) * 18;
+  } else if (fmt == QMM_FMT_Q8_0) {
+    sub.weights = w + (size_t)n_begin * (size_t)(d->K / 32) * 34;
+  } else {
+    sub.weights = w + (size_t)n_begin * (size_t)d->K;
+    if (d->scales) sub.scales = d->scales + (size_t)(n_begin / 128) * (size_t)(d->K / 128);
+  }
+  return qmm_create(out, &sub, stream);
+}
+
 int qmm_destroy(qmm_t h) {
   if (!h) return QMM_OK;
   {
