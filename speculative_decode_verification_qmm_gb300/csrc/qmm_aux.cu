@@ -44,20 +44,45 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
   } else {
     __shared__ float s_max[8];
     __shared__ float s_mul;
-    // pass 1: largest magnitude of the (rotated) values
+    const int warp = tid >> 5;
+    // Splits of up to IT x 1024 elements keep the thread's values in
+    // registers: every load is issued before any is used (one memory round
+    // trip for the whole split) and the values are rotated once.
+    constexpr int IT = 8;
+    const int64_t nit = (kr + 1023) / 1024;
+    const bool resident = nit <= IT;
+    float v[IT][4];
     float amax = 0.f;
-    for (int64_t base = (int64_t)(tid & ~31) * 4; base < kr; base += 256 * 4) {
-      const int64_t kl = base + lane * 4;
-      const int64_t k = k0 + kl;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (k < p.K) load4_bf16(src + k, v);
-      if constexpr (HAD) fwht_lanes<HB>(v, lane);
+    if (resident) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[e]));
+      for (int it = 0; it < IT; ++it) {
+        v[it][0] = v[it][1] = v[it][2] = v[it][3] = 0.f;
+        const int64_t kl = (int64_t)it * 1024 + warp * 128 + lane * 4;
+        if (it < nit && kl < kr && k0 + kl < p.K) load4_bf16(src + k0 + kl, v[it]);
+      }
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        if (it < nit) {  // uniform over the block
+          if constexpr (HAD) fwht_lanes<HB>(v[it], lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[it][e]));
+        }
+      }
+    } else {
+      // pass 1 over a long split: largest magnitude of the (rotated) values
+      for (int64_t base = (int64_t)warp * 128; base < kr; base += 256 * 4) {
+        const int64_t kl = base + lane * 4;
+        const int64_t k = k0 + kl;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (k < p.K) load4_bf16(src + k, x);
+        if constexpr (HAD) fwht_lanes<HB>(x, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
-    if (lane == 0) s_max[tid >> 5] = amax;
+    if (lane == 0) s_max[warp] = amax;
     __syncthreads();
     if (tid == 0) {
       float a = s_max[0];
@@ -74,19 +99,30 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const __grid_constant__ P
     }
     __syncthreads();
     const float mul = s_mul;
-    // pass 2: scale (exact power of two), round to f16, store
-    for (int64_t base = (int64_t)(tid & ~31) * 4; base < kr; base += 256 * 4) {
-      const int64_t kl = base + lane * 4;
-      const int64_t k = k0 + kl;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (k < p.K) load4_bf16(src + k, v);
-      if constexpr (HAD) fwht_lanes<HB>(v, lane);
-      const __half2 h01 = __floats2half2_rn(v[0] * mul, v[1] * mul);
-      const __half2 h23 = __floats2half2_rn(v[2] * mul, v[3] * mul);
+    auto store4 = [&](int64_t kl, const float (&x)[4]) {
+      const __half2 h01 = __floats2half2_rn(x[0] * mul, x[1] * mul);
+      const __half2 h23 = __floats2half2_rn(x[2] * mul, x[3] * mul);
       uint2 o;
       o.x = *reinterpret_cast<const uint32_t*>(&h01);
       o.y = *reinterpret_cast<const uint32_t*>(&h23);
       *reinterpret_cast<uint2*>(p.out + dst_index(kl)) = o;
+    };
+    // pass 2: scale (exact power of two), round to f16, store
+    if (resident) {
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int64_t kl = (int64_t)it * 1024 + warp * 128 + lane * 4;
+        if (it < nit && kl < kr) store4(kl, v[it]);
+      }
+    } else {
+      for (int64_t base = (int64_t)warp * 128; base < kr; base += 256 * 4) {
+        const int64_t kl = base + lane * 4;
+        const int64_t k = k0 + kl;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (k < p.K) load4_bf16(src + k, x);
+        if constexpr (HAD) fwht_lanes<HB>(x, lane);
+        store4(kl, x);
+      }
     }
   }
 }
