@@ -318,6 +318,8 @@ def setup_workload(q, synth, torch, dev, args, workload):
         kernel, dtype, l2 = "verify_kernel<0", "bf16", "inputs larger than L2 (11.6 GiB per pass)"
     else:
         shape_name, hadamard, Ms = WORKLOADS[workload]
+        if getattr(args, "ms", None) and workload == args.workload:
+            Ms = tuple(int(x) for x in args.ms.split(","))
         spec = synth.SHAPES[shape_name]
         N, K = spec["N"], spec["K"]
         one = {"q4_0": N * K // 32 * 18, "q8_0": N * K // 32 * 34}.get(
@@ -1064,6 +1066,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="default workload only: skip the other target configurations")
+    ap.add_argument("--ms", default="",
+                    help="comma-separated drafted-row counts to time instead of the workload's "
+                         "own (for example 1,8,16 on the MLP shapes)")
     ap.add_argument("--shard", action="store_true",
                     help="split each matrix by rows over the ranks and all-gather every "
                          "call's output (strong scaling) instead of running replicas")
