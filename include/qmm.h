@@ -375,6 +375,33 @@ int qmm_debug_set_wait_limit(qmm_t h, int64_t ns);
  * fail as if cudaMalloc had failed (n = 0 disables; the hook fires once). */
 int qmm_debug_fail_allocs(int n);
 
+/* Profiling hook: per-CTA timeline of the warp-level (mma.sync) verify
+ * kernel.  A library built with QMM_TRACE defined has each CTA of each verify
+ * call on h write, at the points below, the device's global timer (ns) into
+ * buf (device, n_words 64-bit words): call c (counted from this call on)
+ * writes slot c % (n_words / slot) of slot = ctas * QMM_TRACE_FIELDS words
+ * (ctas from qmm_get_info), CTA b at words b * QMM_TRACE_FIELDS + field.
+ * buf = NULL switches it off.  The caller owns buf and keeps it alive while
+ * calls that write it may run.  Returns QMM_ERR_STATE if the library was
+ * built without QMM_TRACE (the product build: the stamps are compiled out)
+ * or h is not live, QMM_ERR_INVALID_ARG if buf holds no slot, and
+ * QMM_ERR_SHAPE for a tcgen05 handle (which has no stamps). */
+#define QMM_TRACE_FIELDS 16
+enum {
+  QMM_TR_ENTRY = 0,  /* the CTA's barriers are initialised                    */
+  QMM_TR_SMID = 1,   /* (not a time) the SM the CTA runs on                   */
+  QMM_TR_PDL = 2,    /* the previous kernel's writes are visible (thread 0)   */
+  QMM_TR_DATA = 3,   /* warp 0's first chunk has landed                       */
+  QMM_TR_LOOP = 4,   /* warp 0 has finished its last stage                    */
+  QMM_TR_EPI = 5,    /* every warp has finished its stages                    */
+  QMM_TR_RED = 6,    /* the chunk partials are in shared memory               */
+  QMM_TR_PART = 7,   /* the CTA's result (S = 1) or split partial is written  */
+  QMM_TR_ARRIVE = 8, /* S > 1: the split's arrival add has returned           */
+  QMM_TR_LAST = 9,   /* (not a time) 1 if this split did the fix-up           */
+  QMM_TR_EXIT = 10   /* thread 0 leaves the kernel                            */
+};
+int qmm_debug_set_trace(qmm_t h, uint64_t* buf, int64_t n_words);
+
 #ifdef __cplusplus
 }
 #endif

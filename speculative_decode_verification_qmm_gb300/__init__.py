@@ -23,7 +23,8 @@ __all__ = [
     "Matrix", "qmm_create", "qmm_create_rows", "shard_rows", "qmm_destroy", "qmm_verify", "qmm_verify_greedy", "qmm_verify_host",
     "qmm_verify_noalloc", "qmm_prefill", "qmm_prefill_workspace", "qmm_sync_status",
     "qmm_get_info", "qmm_dequantize", "qmm_hadamard32", "qmm_quantize_q4_0", "qmm_quantize_fp8",
-    "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_strerror", "qmm_last_cuda_error",
+    "qmm_debug_set_wait_limit", "qmm_debug_fail_allocs", "qmm_debug_set_trace", "qmm_strerror",
+    "qmm_last_cuda_error",
     "QmmError", "load",
     "QMM_OK", "QMM_ERR_INVALID_ARG", "QMM_ERR_SHAPE", "QMM_ERR_M_RANGE", "QMM_ERR_ALIGN",
     "QMM_ERR_CUDA", "QMM_ERR_TIMEOUT", "QMM_ERR_STATE", "QMM_ERR_DEVICE",
@@ -224,6 +225,13 @@ def qmm_debug_set_wait_limit(h, ns: int) -> None:
 
 def qmm_debug_fail_allocs(n: int) -> None:
     _check("qmm_debug_fail_allocs", load().qmm_debug_fail_allocs(n))
+
+
+def qmm_debug_set_trace(h, buf=None) -> None:
+    """``buf``: a CUDA int64/uint64 tensor of stamp slots, or None to switch off
+    (libraries built with QMM_TRACE only; see speculative_decode_verification_qmm_gb300.timeline)."""
+    ptr, n = (None, 0) if buf is None else (_ptr(buf), buf.numel())
+    _check("qmm_debug_set_trace", load().qmm_debug_set_trace(h, ptr, n))
 
 
 # ------------------------------------------------------------------ convenience

@@ -93,7 +93,12 @@ SIGNATURES = {
     "qmm_quantize_fp8": (_INT, [_P, _I64, _I64, _U32, _P, _P, _P]),
     "qmm_debug_set_wait_limit": (_INT, [_P, _I64]),
     "qmm_debug_fail_allocs": (_INT, [_INT]),
+    "qmm_debug_set_trace": (_INT, [_P, _P, _I64]),
 }
+
+QMM_TRACE_FIELDS = 16
+(QMM_TR_ENTRY, QMM_TR_SMID, QMM_TR_PDL, QMM_TR_DATA, QMM_TR_LOOP, QMM_TR_EPI, QMM_TR_RED,
+ QMM_TR_PART, QMM_TR_ARRIVE, QMM_TR_LAST, QMM_TR_EXIT) = range(11)
 
 _lib = None
 
@@ -102,14 +107,20 @@ def lib_path() -> str:
     return _build.LIB
 
 
-def load(build_if_missing: bool = False) -> ctypes.CDLL:
-    """Load libqmm.so (optionally building it first) and declare its signatures."""
+def load(build_if_missing: bool = False, path: str | None = None) -> ctypes.CDLL:
+    """Load libqmm.so (optionally building it first) and declare its signatures.
+
+    ``path``: load that build of the library instead (a profiling variant);
+    a process loads one library only."""
     global _lib
     if _lib is not None:
+        if path is not None and os.path.abspath(path) != os.path.abspath(_lib._name):
+            raise RuntimeError(f"libqmm already loaded from {_lib._name}")
         return _lib
-    path = _build.LIB
-    if build_if_missing and not _build.up_to_date():
-        path = _build.build()
+    if path is None:
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            path = _build.build()
     if not os.path.exists(path):
         raise RuntimeError(
             f"libqmm.so is not built ({path} missing); run "

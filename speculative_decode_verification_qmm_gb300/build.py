@@ -40,23 +40,30 @@ def _inputs():
             + [os.path.join(INCLUDE, "qmm.h")])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str | None = None) -> bool:
+    lib = LIB if lib is None else lib
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile the CUDA library if needed and return the path of ``libqmm.so``."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir=None) -> str:
+    """Compile the CUDA library if needed and return the path of ``libqmm.so``.
+
+    ``out_dir``: build a variant (for example with ``extra_flags=["-DQMM_TRACE"]``)
+    into that folder instead (one set of flags per folder: the up-to-date check
+    compares times only); the in-tree library is untouched."""
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libqmm.so")
+    odir = OUT_DIR if out_dir is None else out_dir
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(odir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for s in SOURCES:
-        obj = os.path.join(OUT_DIR, s.replace(".cu", ".o"))
+        obj = os.path.join(odir, s.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, s), "-o", obj]
         if verbose:
@@ -72,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             print(out, file=sys.stderr)
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -72,6 +72,11 @@ struct qmm_handle {
   float* stage_out = nullptr;     // [MAX_M][N]
   uint64_t wait_limit_ns = DEFAULT_WAIT_LIMIT_NS;
   int last_cuda_error = 0;
+  // qmm_debug_set_trace (builds with QMM_TRACE): the caller's stamp buffer,
+  // its slot count and the verify calls made since it was set
+  unsigned long long* trace = nullptr;
+  int64_t trace_slots = 0;
+  int64_t trace_calls = 0;
   // Tensor maps over the activation rows of recent calls, keyed by what they
   // encode (a graph captures the map by value, so an entry can be reused or
   // replaced freely).
@@ -632,6 +637,11 @@ int verify_impl(qmm_t h, const uint16_t* act, int64_t lda, float* out, int64_t l
   vp.argmax_out = nullptr;
   vp.accept_out = nullptr;
   vp.n_tiles = p.n_tiles;
+  vp.trace = nullptr;
+  if (h->trace) {
+    const int64_t slot = (int64_t)p.n_tiles * p.S * QMM_TRACE_FIELDS;
+    vp.trace = h->trace + (h->trace_calls++ % h->trace_slots) * slot;
+  }
   if (g) {
     vp.best = h->greedy;
     vp.tiles_done = reinterpret_cast<int*>(h->greedy + MAX_M);
@@ -921,6 +931,26 @@ int qmm_debug_set_wait_limit(qmm_t h, int64_t ns) {
   if (ns < 0) return QMM_ERR_INVALID_ARG;
   h->wait_limit_ns = (uint64_t)ns;
   return QMM_OK;
+}
+
+int qmm_debug_set_trace(qmm_t h, uint64_t* buf, int64_t n_words) {
+#ifndef QMM_TRACE
+  (void)buf;
+  (void)n_words;
+  return QMM_ERR_STATE;  // the stamps are compiled out of this build
+#else
+  if (!is_live(h)) return QMM_ERR_STATE;
+  if (h->plan.tc) return QMM_ERR_SHAPE;
+  h->trace = nullptr;
+  h->trace_slots = 0;
+  h->trace_calls = 0;
+  if (!buf) return QMM_OK;
+  const int64_t slot = (int64_t)h->plan.n_tiles * h->plan.S * QMM_TRACE_FIELDS;
+  if (n_words < slot) return QMM_ERR_INVALID_ARG;
+  h->trace = reinterpret_cast<unsigned long long*>(buf);
+  h->trace_slots = n_words / slot;
+  return QMM_OK;
+#endif
 }
 
 }  // extern "C"

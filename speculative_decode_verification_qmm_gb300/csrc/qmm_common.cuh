@@ -44,6 +44,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "qmm.h"
+
 namespace qmm {
 
 constexpr int TILE_N = 128;           // rows of W per CTA tile
@@ -99,6 +101,9 @@ struct VerifyParams {
   int32_t* argmax_out;       // [M] first row of the largest score of each drafted row
   int32_t* accept_out;       // [2] accepted drafts k, then argmax_out[k]
   int n_tiles;               // row tiles of the call
+  // Builds with QMM_TRACE: per-CTA timeline of this call, [CTA][QMM_TRACE_FIELDS]
+  // global-timer stamps (NULL: none).  The product build compiles the stamps out.
+  unsigned long long* trace;
 };
 
 struct PrepParams {
@@ -113,6 +118,19 @@ struct PrepParams {
   int spc;
   int stage_k;
 };
+
+// Per-CTA timeline stamp (builds with QMM_TRACE only; the field indices are
+// QMM_TR_* of qmm.h).
+#ifdef QMM_TRACE
+#define QMM_STAMP(p, field, value)                                                   \
+  do {                                                                               \
+    if ((p).trace) (p).trace[(size_t)blockIdx.x * QMM_TRACE_FIELDS + (field)] = (value); \
+  } while (0)
+#else
+#define QMM_STAMP(p, field, value) \
+  do {                             \
+  } while (0)
+#endif
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -155,6 +173,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

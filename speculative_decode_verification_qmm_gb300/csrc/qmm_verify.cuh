@@ -420,6 +420,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  if (tid == 0) {
+    QMM_STAMP(p, QMM_TR_ENTRY, global_timer_ns());
+    QMM_STAMP(p, QMM_TR_SMID, sm_id());
+  }
   // Let the next kernel in the stream start its prologue (weight prefetch).
   pdl_trigger();
 
@@ -474,6 +478,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       for (int c = 0; c < NCH; ++c) request(i, c, true, false);
     // Activations may be written by the previous kernel: wait for it.
     pdl_wait();
+    QMM_STAMP(p, QMM_TR_PDL, global_timer_ns());
     for (int i = 0; i < pre; ++i)
       for (int c = 0; c < NCH; ++c) request(i, c, false, true);
   }
@@ -511,6 +516,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           s_flag[0] = 1;
           break;
         }
+        if (i == 0 && warp == 0 && lane == 0) QMM_STAMP(p, QMM_TR_DATA, global_timer_ns());
         const uint32_t wch = s_w + slot * F::STAGE_BYTES + chunk * F::CHUNK_BYTES +
                              sub0 * F::UNIT_BYTES;
         const uint32_t ach = s_a + slot * L::A_STAGE + chunk * L::A_CHUNK;
@@ -525,6 +531,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         __syncwarp();
         if (s_flag[0]) break;
       }
+      if (warp == 0 && lane == 0) QMM_STAMP(p, QMM_TR_LOOP, global_timer_ns());
     } else {
       using T = typename std::conditional<std::is_same<Op, Bf16Op>::value, __nv_bfloat16,
                                           __half>::type;
@@ -551,6 +558,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
   __syncthreads();
+  if (tid == 0) QMM_STAMP(p, QMM_TR_EPI, global_timer_ns());
   const bool aborted = s_flag[0] != 0;
   if (aborted) {
     // Give up: no copy requested by this CTA may still be landing in shared
@@ -608,6 +616,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
   __syncthreads();
+  if (tid == 0) QMM_STAMP(p, QMM_TR_RED, global_timer_ns());
 
   // The CTA's partial: the chunk partials added in chunk order, times the
   // pre-pass's factor of this (row, split).  With one split it is the result;
@@ -631,10 +640,12 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
   if (p.S == 1) {
+    if (tid == 0) QMM_STAMP(p, QMM_TR_PART, global_timer_ns());
     if constexpr (GREEDY) {
       __syncthreads();  // fin complete
       greedy_tile(p, fin, tile, M, !aborted, tid, s_flag);
     }
+    if (tid == 0) QMM_STAMP(p, QMM_TR_EXIT, global_timer_ns());
     return;
   }
 
@@ -647,6 +658,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // threads ordered after it by the second barrier.
   __syncthreads();
   if (tid == 0) {
+    QMM_STAMP(p, QMM_TR_PART, global_timer_ns());
     int prev;
     asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
                  : "=r"(prev)
@@ -655,6 +667,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     const bool last = prev == p.S - 1;
     if (last) p.counters[tile] = 0;
     s_flag[1] = last ? 1 : 0;
+    QMM_STAMP(p, QMM_TR_ARRIVE, global_timer_ns());
+    QMM_STAMP(p, QMM_TR_LAST, last ? 1ull : 0ull);
   }
   __syncthreads();
   if (s_flag[1] && !aborted) {
@@ -687,6 +701,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       greedy_tile(p, fin, tile, M, !aborted, tid, s_flag);
     }
   }
+  if (tid == 0) QMM_STAMP(p, QMM_TR_EXIT, global_timer_ns());
 }
 
 }  // namespace qmm
