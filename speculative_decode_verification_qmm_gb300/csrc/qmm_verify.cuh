@@ -676,14 +676,36 @@ __global__ void __launch_bounds__(THREADS, 2)
     // float4 piece q: drafted row q / 32, rows 4 (q % 32) .. + 3
     for (int q = tid; q < M * (TILE_N / 4); q += THREADS) {
       const int m = q / (TILE_N / 4), row = 4 * (q % (TILE_N / 4));
-      float4 v = __ldcg(reinterpret_cast<const float4*>(base + m * TILE_N + row));
-      for (int sp = 1; sp < p.S; ++sp) {
-        const float4 x =
-            __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)sp * MAX_M + m) * TILE_N + row));
-        v.x += x.x;
-        v.y += x.y;
-        v.z += x.z;
-        v.w += x.w;
+      float4 v;
+      if (NT8 == 2 && p.S <= 8) {
+        // 9-16 drafted rows: every split's piece is requested before the
+        // first add (one round trip to L2), then added in split order, as
+        // below.  (At 8 rows and fewer the plain loop measured faster on
+        // 5120 x 5120; here it saves 4 % of a down call at 16 rows.)
+        float4 x[8];
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp)
+          if (sp < p.S)
+            x[sp] = __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)sp * MAX_M + m) * TILE_N + row));
+        v = x[0];
+#pragma unroll
+        for (int sp = 1; sp < 8; ++sp)
+          if (sp < p.S) {
+            v.x += x[sp].x;
+            v.y += x[sp].y;
+            v.z += x[sp].z;
+            v.w += x[sp].w;
+          }
+      } else {
+        v = __ldcg(reinterpret_cast<const float4*>(base + m * TILE_N + row));
+        for (int sp = 1; sp < p.S; ++sp) {
+          const float4 x =
+              __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)sp * MAX_M + m) * TILE_N + row));
+          v.x += x.x;
+          v.y += x.y;
+          v.z += x.z;
+          v.w += x.w;
+        }
       }
       const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
