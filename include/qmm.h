@@ -53,7 +53,9 @@
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Calls documented as asynchronous only enqueue work on it.
  *   - The caller owns every buffer it passes; the library never frees caller
- *     memory and keeps no pointer to it after the call returns.
+ *     memory and keeps no pointer to it after the call returns (the one
+ *     exception is the stamp buffer of the profiling hook qmm_debug_set_trace,
+ *     kept until it is switched off or the handle is destroyed).
  *   - bf16 activations are passed as uint16_t bit patterns.
  */
 #ifndef QMM_H_
