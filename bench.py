@@ -986,9 +986,20 @@ def oracle_sample_rate(budget_s: float, workload: str):
 
 
 def cpu_baseline(args):
+    """The oracle on all host cores (the reported baseline) and, beside it, on
+    one thread with a shorter budget."""
+    import oracle as O
     v, cores, sample = oracle_sample_rate(args.cpu_budget, args.workload)
-    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    line = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": sample}
+    try:
+        O.set_num_threads(1)
+        v1, _, sample1 = oracle_sample_rate(min(3.0, args.cpu_budget / 3), args.workload)
+        line["single_thread"] = {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                                 "sample": sample1}
+    finally:
+        O.set_num_threads(cores)
+    return line
 
 
 def run_reference(args, ws, rank):
